@@ -1,0 +1,397 @@
+"""Benchmark of fused SDPA training (forward + backward) on GB300.
+
+One step = sdpa_fwd + sdpa_bwd (the whole hot path) on the long-context
+decoder workload B8 H16 S4096 D128, causal, bf16, dropout 0 (seeded
+synthetic inputs, BHSE). Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+value       whole-job TFLOP/s of the step (algorithmic flops: forward 4*D*pairs,
+            backward 10*D*pairs per head, pairs = unmasked (query, key) pairs)
+            with inputs resident in HBM; the bf16 fraction of the measured
+            tensor peak is reported beside it.
+e2e         the same metric through the public API with host buffers: each
+            step copies q, k, v, dout from pinned host memory and copies out,
+            lse, dq, dk, dv back.
+roofline    the backward (dominant) and forward kernels against the measured
+            dense bf16 peak.
+cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
+            the same workload (whole heads), on this host's cores.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "decoder_long"
+METRIC = "fwd/bwd TFLOP/s bf16 (B8 H16 S4096 D128 causal); % of GB300 BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def pairs(w):
+    """Unmasked (query, key) pairs per head; causal is top-left aligned."""
+    if not w.is_causal:
+        return w.Sq * w.Sk
+    n = min(w.Sq, w.Sk)
+    full = w.Sq - n  # rows that see every key
+    return n * (n + 1) // 2 + full * w.Sk
+
+
+def flops(w):
+    p = pairs(w) * w.B * w.H * w.D
+    return 4 * p, 10 * p
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": f"{w.name} B{w.B} H{w.H} Sq{w.Sq} Sk{w.Sk} D{w.D} "
+                       f"{'causal' if w.is_causal else 'full'} p{w.dropout_p} bf16 BHSE",
+           "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "causal": w.is_causal,
+           "dropout_p": w.dropout_p, "layout": "BHSE",
+           "l2": "inputs larger than L2 (q,k,v,dout,out 134 MB each; ~1.1 GB per step), no flush"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "scaled_dot_product_07_gb300", "csrc", ent["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return ent["bytes_per_launch"] if digest == ent.get("source_sha256_16") else None
+
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier_max(value, world):
+    """Max over ranks (host float) after a barrier."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+_INPUT_CACHE = {}
+
+
+def cached_inputs(w):
+    from scaled_dot_product_07_gb300 import workloads as W
+    if w.name not in _INPUT_CACHE:
+        _INPUT_CACHE[w.name] = W.draw_inputs(w)
+    return _INPUT_CACHE[w.name]
+
+
+def run_oracle_sample(w, budget_s, min_heads=1, start=0):
+    """Oracle forward + backward on whole heads until `budget_s` of CPU time."""
+    import numpy as np
+
+    import oracle
+    q, k, v, do = cached_inputs(w)
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    heads = heads[start % len(heads):] + heads[:start % len(heads)]
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        qh, kh, vh, doh = f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), f64(do[b, h])
+        scale = oracle.default_scale(w.D)
+        out, lse = oracle.head_forward(qh, kh, vh, b, h, w.H, w.dropout_p, w.is_causal, scale,
+                                       w.seed, w.offset)
+        oracle.head_backward(doh, qh, kh, vh, out, lse, b, h, w.H, w.dropout_p, w.is_causal,
+                             scale, w.seed, w.offset, check_delta=False)
+        done += 1
+        if done >= min_heads and time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    f = sum(flops(w)) / (w.B * w.H) * done
+    return f / el / 1e12, done, el
+
+
+def cpu_threads():
+    return os.cpu_count() or 1
+
+
+def bench_reference(args, w):
+    rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    # each step: the oracle's fwd+bwd of one whole head of the workload
+    cached_inputs(w)
+    for i in range(args.warmup):
+        run_oracle_sample(w, 0.0, 1, start=i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run_oracle_sample(w, 0.0, 1, start=args.warmup + i)
+    el = time.perf_counter() - t0
+    val = sum(flops(w)) / (w.B * w.H) * args.steps / el / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, {"sample": "one whole head per step"}),
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} heads (fwd+bwd, fp64 numpy) of {w.B * w.H}"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def bench_ours(args, w):
+    import torch
+
+    import scaled_dot_product_07_gb300 as sdpa
+    from scaled_dot_product_07_gb300 import workloads as W
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from scaled_dot_product_07_gb300 import _build
+    _build.build()
+    sdpa.load_library()
+
+    inputs_cpu = cached_inputs(w)
+    q, k, v, do = (x.to(dev) for x in inputs_cpu)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(sdpa.sdpa_bwd_workspace_size(w.B, w.H, w.Sq, w.Sk, w.D), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sdpa.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset, out=out, lse=lse)
+        sdpa.sdpa_bwd(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
+                      dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if sdpa.sdpa_check_device() != 0:
+        raise RuntimeError("kernel wait timed out during warm-up")
+
+    # ---- timed region: K whole steps, per-phase events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        sdpa.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset, out=out, lse=lse)
+        ev[i][1].record(stream)
+        sdpa.sdpa_bwd(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
+                      dq=dq, dk=dk, dv=dv, workspace=ws)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if sdpa.sdpa_check_device() != 0:
+        raise RuntimeError("kernel wait timed out in the timed region")
+    total_ms = barrier_max(t_start.elapsed_time(t_end), world)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    f_fwd, f_bwd = flops(w)
+    step_ms = total_ms / args.steps
+    value = world * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+    peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hdo = (pin(x) for x in inputs_cpu)
+    hout, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, q, k, v))
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (hout, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        dq_, dk_, dv_ = (x.to(dev, non_blocking=True) for x in (hq, hk, hv))
+        ddo = hdo.to(dev, non_blocking=True)
+        o, l, s_, off_ = sdpa.sdpa_fwd(dq_, dk_, dv_, w.dropout_p, w.is_causal, None, w.seed, w.offset)
+        g = sdpa.sdpa_bwd(ddo, dq_, dk_, dv_, o, l, w.dropout_p, w.is_causal, s_, off_, None)
+        for src, dst in zip((o, l) + g, (hout, hlse, hdq, hdk, hdv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = barrier_max(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_val = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return 0
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        val, heads, el = run_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{heads} whole heads of {w.B * w.H} (fwd+bwd, fp64 numpy, {el:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w),
+        "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
+        "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak,
+                "note": "preprocess + main + dQ-convert kernels"},
+        "pct_of_bf16_peak": 100.0 * (value / world) / peak,
+        "roofline": {"kernel": "bwd_main_kernel (timed with its preprocess and dQ-convert launches)",
+                     "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": bwd_tf / peak, "traffic": kernel_traffic("bwd_main_kernel"),
+                     "peak_source": f"{pk_src} bf16_tflops (burst)"},
+        "roofline_fwd": {"kernel": "fwd_kernel", "bound": "tensor", "achieved": fwd_tf, "peak": peak,
+                         "unit": "TFLOP/s", "frac": fwd_tf / peak,
+                         "traffic": kernel_traffic("fwd_kernel"),
+                         "peak_source": f"{pk_src} bf16_tflops (burst)"},
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from scaled_dot_product_07_gb300 import workloads as W
+    w = W.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,154 @@
+/*
+ * sdpa.h — C ABI of the GB300 (sm_103a) fused scaled-dot-product attention
+ * library for training: a flash-style forward that stashes the per-row
+ * log-sum-exp, and the matching backward that recomputes the probabilities
+ * from it.
+ *
+ * The operation is scaled dot-product attention as named in the
+ * "Scaled_dot_product_attention" thread (discuss.pytorch.org):
+ *     out = dropout(softmax(scale * Q K^T + causal)) V
+ * with the argument lists of sdpfa_fwd / sdpfa_bwd in test_sdpa_loop_split
+ * ("DID loop split for SDPA", NVIDIA/Fuser PR 3711), the E = Ev restriction
+ * of the SdpaFwdOp plan (NVIDIA/Fuser issue 2278, "Note to self: next PRs"),
+ * and dropout regenerated from (seed, offset) and the absolute element index
+ * ("REDO of dropout support for mem eff #102038", pytorch PR 103704, Summary).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are described by sdpa_tensor: a device pointer to bfloat16 data,
+ *   the LOGICAL shape [B, H, S, D] and the stride of each logical dim in
+ *   ELEMENTS. Any dense order of B, H, S works as long as D is innermost
+ *   (stride[3] == 1); BHSE (stride order 3,2,1,0) and BSHE (3,1,2,0) are the
+ *   two layouts of test_sdpa_loop_split. Strides of dims of size > 1 must be
+ *   multiples of 8 elements (16 bytes) and every base pointer 16-byte aligned.
+ * - D (= E = Ev, the head dim of q, k and v) must be 64 or 128.
+ * - Causal masking is top-left aligned: key j is visible to query i iff j <= i.
+ * - Ownership: the caller allocates every input, output and workspace; the
+ *   library allocates no device memory and keeps no per-call state. Work is
+ *   enqueued on `stream` (0 = legacy default stream) and the call returns
+ *   without synchronising. Inputs must stay valid until the stream reaches
+ *   the work.
+ * - Errors: argument problems are reported synchronously and nothing is
+ *   launched. SDPA_ERR_CUDA means a launch failed (the CUDA error is
+ *   retrievable with cudaGetLastError). Every wait inside the kernels is
+ *   bounded; a kernel whose wait runs out records it in a device error word,
+ *   which sdpa_check_device() reads (and the entry points read themselves
+ *   when the environment variable SDPA_DEBUG_SYNC=1 is set).
+ * - Empty problems (B*H*Sq == 0) succeed without launching anything, except
+ *   that the backward still zero-fills dk and dv when Sq == 0.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (binary-compatible with cudaStream_t). */
+typedef struct CUstream_st* sdpa_stream_t;
+
+typedef struct {
+  void* data;          /* device pointer, bfloat16 elements */
+  int64_t size[4];     /* logical [B, H, S, D] */
+  int64_t stride[4];   /* element strides of the logical dims */
+} sdpa_tensor;
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,    /* shape mismatch, null pointer, p outside [0,1), bad scale */
+  SDPA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, D not innermost */
+  SDPA_ERR_ALIGNMENT = 3,      /* base or stride not 16-byte aligned */
+  SDPA_ERR_CUDA = 4,           /* a CUDA launch or driver call failed */
+  SDPA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up on a bounded wait */
+  SDPA_ERR_WORKSPACE = 6       /* workspace missing or smaller than required */
+} sdpa_status;
+
+/*
+ * sdpa_fwd — forward of fused attention for training (sdpfa_fwd of
+ * test_sdpa_loop_split, "DID loop split for SDPA"; the stashed log-sum-exp
+ * of issue "SdpaOpFwd / SdpaOpBwd nodes", NVIDIA/Fuser 2278).
+ *   q [B,H,Sq,D], k [B,H,Sk,D], v [B,H,Sk,D]: inputs (read only).
+ *   dropout_p in [0,1): probability of dropping an attention weight;
+ *     kept weights are scaled by 1/(1-p).
+ *   is_causal: nonzero for the top-left causal mask.
+ *   scale: softmax scale (> 0, finite); the usual choice is 1/sqrt(D).
+ *   seed, offset: Philox4x32-10 key and counter offset of the dropout mask
+ *     (ignored when dropout_p == 0). Pass the same values to sdpa_bwd.
+ *   out [B,H,Sq,D]: bfloat16 output, any layout allowed for q.
+ *   lse: float32 [B,H,Sq], contiguous: natural-log log-sum-exp of each
+ *     scaled, masked score row (before dropout).
+ * Requires Sk >= 1 whenever B*H*Sq > 0.
+ */
+sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                     double dropout_p, int is_causal, float scale, uint64_t seed,
+                     uint64_t offset, sdpa_tensor* out, float* lse, sdpa_stream_t stream);
+
+/*
+ * sdpa_bwd_workspace_size — bytes of device workspace sdpa_bwd needs for
+ * this problem size: an fp32 dQ accumulator and two fp32 row vectors, with
+ * Sq rounded up to a multiple of 128. Returns 0 for an empty problem.
+ */
+size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D);
+
+/*
+ * sdpa_bwd — backward of fused attention (sdpfa_bwd of test_sdpa_loop_split,
+ * "DID loop split for SDPA"): recomputes the probabilities from lse,
+ * regenerates the dropout mask from (seed, offset), and writes
+ *   dq = scale * dS K,  dk = scale * dS^T Q,  dv = P~^T dout,
+ * with dS = P * (dout V^T * keep/(1-p) - rowsum(dout * out)).
+ *   dout, q, k, v, out: bfloat16 tensors as in sdpa_fwd (out and lse must be
+ *     the forward's results for the same q, k, v, p, is_causal, seed, offset, scale).
+ *   lse: float32 [B,H,Sq] contiguous, from sdpa_fwd.
+ *   dq [B,H,Sq,D], dk, dv [B,H,Sk,D]: bfloat16 outputs (any allowed layout).
+ *   workspace: device memory of at least sdpa_bwd_workspace_size() bytes,
+ *     256-byte aligned; its contents on entry do not matter and are
+ *     overwritten. It must not be shared by calls in flight at the same time.
+ * Launches three kernels on `stream`: preprocess, main, dQ conversion.
+ */
+sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                     const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                     double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                     float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                     void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
+
+/*
+ * sdpa_dropout_mask_debug — writes the keep mask (1 = kept, 0 = dropped) of
+ * every element of a [B,H,Sq,Sk] attention problem into `mask` (uint8, device,
+ * contiguous [B,H,Sq,Sk]), computed by the same device Philox routine the
+ * forward and backward kernels use ("REDO of dropout support for mem eff
+ * #102038", Summary: absolute-index RNG). For tests and debugging.
+ */
+sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                    double dropout_p, uint64_t seed, uint64_t offset,
+                                    uint8_t* mask, sdpa_stream_t stream);
+
+/*
+ * sdpa_check_device — synchronises `stream`, then reports whether any kernel
+ * of this library on the current device gave up on a bounded wait since the
+ * last check (SDPA_ERR_DEVICE_TIMEOUT; the word is cleared) or the stream
+ * reported a CUDA error (SDPA_ERR_CUDA). The pages have no counterpart: this
+ * is the library's failure-detection hook.
+ */
+sdpa_status sdpa_check_device(sdpa_stream_t stream);
+
+/*
+ * sdpa_selftest_wait_timeout — launches one tiny kernel that waits, with the
+ * given bound in nanoseconds, on an mbarrier that nothing ever arrives on,
+ * then synchronises and returns SDPA_ERR_DEVICE_TIMEOUT if the wait gave up
+ * as designed (SDPA_OK would mean the barrier completed, which cannot
+ * happen). It exercises the bounded-wait path without faulting or hanging
+ * the GPU. No counterpart on the pages.
+ */
+sdpa_status sdpa_selftest_wait_timeout(uint64_t limit_ns, sdpa_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sdpa_status_string(sdpa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,250 @@
+"""Fused scaled-dot-product attention for training on GB300 (sm_103a).
+
+Python binding of the C ABI declared in ``include/sdpa.h``. Every function
+here only marshals arguments (torch tensors -> pointers, sizes and strides,
+torch's current CUDA stream) and calls the shared library built from
+``csrc/``; all computation happens in the library's CUDA kernels. PyTorch
+provides device memory and streams. There is no CPU fallback: if the
+library is missing or no GPU is present the calls raise.
+
+    out, lse, seed, offset = sdpa_fwd(q, k, v, dropout_p, is_causal, scale)
+    dq, dk, dv = sdpa_bwd(dout, q, k, v, out, lse, dropout_p, is_causal,
+                          seed, offset, scale)
+
+Tensors have the logical shape [B, H, S, D] (D = 64 or 128, innermost and
+contiguous) in bfloat16, in any dense order of B, H, S with 16-byte aligned
+strides -- e.g. BHSE or BSHE ("DID loop split for SDPA", NVIDIA/Fuser PR
+3711, test_sdpa_loop_split). ``lse`` is float32 [B, H, Sq].
+"""
+
+import ctypes
+import math
+import os
+
+__all__ = [
+    "SdpaError", "load_library", "library_path", "sdpa_fwd", "sdpa_bwd",
+    "sdpa_bwd_workspace_size", "sdpa_dropout_mask_debug", "sdpa_check_device",
+    "sdpa_selftest_wait_timeout", "sdpa_status_string", "SDPAFunction", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libsdpa_gb300.so")
+_LIB = None
+
+# Every entry point of include/sdpa.h.
+EXPORTED_SYMBOLS = (
+    "sdpa_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_dropout_mask_debug",
+    "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string",
+)
+
+SDPA_OK = 0
+STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
+                3: "SDPA_ERR_ALIGNMENT", 4: "SDPA_ERR_CUDA", 5: "SDPA_ERR_DEVICE_TIMEOUT",
+                6: "SDPA_ERR_WORKSPACE"}
+
+
+class SdpaError(RuntimeError):
+    """A library call returned a non-zero status."""
+
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {sdpa_status_string(status)}")
+
+
+class SdpaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("size", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library(path=None):
+    """Load the CUDA library (once). Raises if it has not been built."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    lib = ctypes.CDLL(p)
+    P = ctypes.POINTER(SdpaTensor)
+    i64, u64, dbl, flt, vp = (ctypes.c_int64, ctypes.c_uint64, ctypes.c_double,
+                              ctypes.c_float, ctypes.c_void_p)
+    lib.sdpa_fwd.argtypes = [P, P, P, dbl, ctypes.c_int, flt, u64, u64, P, vp, vp]
+    lib.sdpa_fwd.restype = ctypes.c_int
+    lib.sdpa_bwd_workspace_size.argtypes = [i64, i64, i64, i64, i64]
+    lib.sdpa_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.sdpa_bwd.argtypes = [P, P, P, P, P, vp, dbl, ctypes.c_int, u64, u64, flt, P, P, P, vp,
+                             ctypes.c_size_t, vp]
+    lib.sdpa_bwd.restype = ctypes.c_int
+    lib.sdpa_dropout_mask_debug.argtypes = [i64, i64, i64, i64, dbl, u64, u64, vp, vp]
+    lib.sdpa_dropout_mask_debug.restype = ctypes.c_int
+    lib.sdpa_check_device.argtypes = [vp]
+    lib.sdpa_check_device.restype = ctypes.c_int
+    lib.sdpa_selftest_wait_timeout.argtypes = [u64, vp]
+    lib.sdpa_selftest_wait_timeout.restype = ctypes.c_int
+    lib.sdpa_status_string.argtypes = [ctypes.c_int]
+    lib.sdpa_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def sdpa_status_string(status):
+    return load_library().sdpa_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != SDPA_OK:
+        raise SdpaError(status, where)
+
+
+def _desc(t):
+    """Descriptor of a logical [B,H,S,D] tensor (pointer, sizes, element strides)."""
+    if t.dim() != 4:
+        raise ValueError("expected a 4-D tensor [B, H, S, D]")
+    d = SdpaTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    for i in range(4):
+        d.size[i] = t.size(i)
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_tensor(t, name):
+    import torch
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+
+
+def _default_scale(D, scale):
+    return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def sdpa_fwd(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=None, offset=None,
+             out=None, lse=None):
+    """Forward. Returns (out, lse, seed, offset).
+
+    ``scale=None`` uses 1/sqrt(D). When dropout is on and ``seed``/``offset``
+    are not given, the seed is drawn from torch's default CPU generator and
+    the offset is 0; pass the returned values to :func:`sdpa_bwd`.
+    """
+    import torch
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    B, H, Sq, D = q.shape
+    if seed is None:
+        seed = int(torch.randint(0, 2**62, (1,)).item()) if dropout_p > 0 else 0
+    if offset is None:
+        offset = 0
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(out)
+    st = lib.sdpa_fwd(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), float(dropout_p),
+                      int(bool(is_causal)), _default_scale(D, scale), int(seed), int(offset),
+                      ctypes.byref(do_), ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                      _stream(q.device))
+    _check(st, "sdpa_fwd")
+    return out, lse, seed, offset
+
+
+def sdpa_bwd_workspace_size(B, H, Sq, Sk, D):
+    return int(load_library().sdpa_bwd_workspace_size(B, H, Sq, Sk, D))
+
+
+def sdpa_bwd(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
+             scale=None, dq=None, dk=None, dv=None, workspace=None):
+    """Backward. Returns (dq, dk, dv) in the layouts of q, k, v."""
+    import torch
+    lib = load_library()
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_tensor(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = sdpa_bwd_workspace_size(B, H, Sq, Sk, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    descs = [_desc(t) for t in (dout, q, k, v, out, dq, dk, dv)]
+    refs = [ctypes.byref(d) for d in descs]
+    st = lib.sdpa_bwd(refs[0], refs[1], refs[2], refs[3], refs[4],
+                      ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                      float(dropout_p), int(bool(is_causal)), int(seed), int(offset),
+                      _default_scale(D, scale), refs[5], refs[6], refs[7],
+                      ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                      _stream(q.device))
+    _check(st, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def sdpa_dropout_mask_debug(B, H, Sq, Sk, dropout_p, seed, offset, device="cuda"):
+    """uint8 keep mask [B,H,Sq,Sk] from the device Philox routine of the kernels."""
+    import torch
+    lib = load_library()
+    mask = torch.empty((B, H, Sq, Sk), dtype=torch.uint8, device=device)
+    st = lib.sdpa_dropout_mask_debug(B, H, Sq, Sk, float(dropout_p), int(seed), int(offset),
+                                     ctypes.c_void_p(mask.data_ptr() if mask.numel() else None),
+                                     _stream(mask.device))
+    _check(st, "sdpa_dropout_mask_debug")
+    return mask
+
+
+def sdpa_check_device(device="cuda"):
+    """Synchronise and return the status of the library's bounded waits (int)."""
+    return int(load_library().sdpa_check_device(_stream(device)))
+
+
+def sdpa_selftest_wait_timeout(limit_ns=50_000_000, device="cuda"):
+    """Run the bounded-wait self test; returns the status (5 = timed out as designed)."""
+    return int(load_library().sdpa_selftest_wait_timeout(int(limit_ns), _stream(device)))
+
+
+def _make_function():
+    import torch
+
+    class SDPAFunction(torch.autograd.Function):
+        """autograd wrapper: forward = sdpa_fwd, backward = sdpa_bwd."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=None):
+            out, lse, seed, offset = sdpa_fwd(q, k, v, dropout_p, is_causal, scale, seed)
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.args = (dropout_p, is_causal, seed, offset, scale)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            p, causal, seed, offset, scale = ctx.args
+            dq, dk, dv = sdpa_bwd(dout.contiguous(), q, k, v, out, lse, p, causal, seed, offset,
+                                  scale)
+            return dq, dk, dv, None, None, None, None
+
+    return SDPAFunction
+
+
+class _LazyFunction:
+    _fn = None
+
+    def __getattr__(self, name):
+        if _LazyFunction._fn is None:
+            _LazyFunction._fn = _make_function()
+        return getattr(_LazyFunction._fn, name)
+
+
+SDPAFunction = _LazyFunction()

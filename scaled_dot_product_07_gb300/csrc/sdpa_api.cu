@@ -1,0 +1,388 @@
+// C-ABI entry points (include/sdpa.h): argument validation, TMA tensor maps
+// for the caller's strided [B,H,S,D] tensors, and kernel launches on the
+// caller's stream. The library allocates no device memory.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sdpa.h"
+#include "common.cuh"
+
+namespace sdpa {
+namespace {
+
+// Device error word: the first bounded wait that gives up records its site.
+__device__ uint32_t g_wait_error;
+
+// ------------------------------------------------------------ small kernels
+
+__global__ void __launch_bounds__(256) dropout_mask_kernel(int64_t total, uint32_t threshold,
+                                                           PhiloxKey pk, uint8_t* mask) {
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < total;
+       n += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    mask[n] = keep_one(static_cast<uint64_t>(n), threshold, pk) ? 1 : 0;
+}
+
+__global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_word;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_word = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{&abort_word, err, limit_ns};
+    mbar_wait(&bar, 0, wc, kSiteSelftest);  // nothing arrives: gives up after limit_ns
+  }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------ host helpers
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+uint32_t* error_word() {
+  static uint32_t* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wait_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* e = std::getenv("SDPA_WAIT_LIMIT_MS");
+    double ms = e ? std::atof(e) : 2000.0;
+    if (!(ms > 0.0)) ms = 2000.0;
+    return static_cast<uint64_t>(ms * 1e6);
+  }();
+  return v;
+}
+
+bool debug_sync() {
+  static bool v = [] {
+    const char* e = std::getenv("SDPA_DEBUG_SYNC");
+    return e && e[0] == '1';
+  }();
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape of one tensor argument, checked against expected [B,H,S,D].
+sdpa_status check_tensor(const sdpa_tensor* t, int64_t B, int64_t H, int64_t S, int64_t D) {
+  if (!t) return SDPA_ERR_INVALID_ARG;
+  if (t->size[0] != B || t->size[1] != H || t->size[2] != S || t->size[3] != D)
+    return SDPA_ERR_INVALID_ARG;
+  const int64_t numel = B * H * S * D;
+  if (numel == 0) return SDPA_OK;
+  if (!t->data) return SDPA_ERR_INVALID_ARG;
+  if (t->stride[3] != 1 && D > 1) return SDPA_ERR_UNSUPPORTED;
+  for (int d = 0; d < 3; ++d) {
+    if (t->size[d] > 1) {
+      if (t->stride[d] <= 0) return SDPA_ERR_INVALID_ARG;
+      if ((t->stride[d] * 2) % 16 != 0) return SDPA_ERR_ALIGNMENT;
+    }
+  }
+  if (!aligned16(t->data)) return SDPA_ERR_ALIGNMENT;
+  return SDPA_OK;
+}
+
+sdpa_status check_dims(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v) {
+  if (!q || !k || !v) return SDPA_ERR_INVALID_ARG;
+  for (int d = 0; d < 4; ++d)
+    if (q->size[d] < 0 || k->size[d] < 0 || v->size[d] < 0) return SDPA_ERR_INVALID_ARG;
+  const int64_t B = q->size[0], H = q->size[1], Sk = k->size[2];
+  if (k->size[0] != B || k->size[1] != H || v->size[0] != B || v->size[1] != H ||
+      v->size[2] != Sk)
+    return SDPA_ERR_INVALID_ARG;
+  // E = Ev: q, k and v share the head dim
+  if (k->size[3] != q->size[3] || v->size[3] != q->size[3]) return SDPA_ERR_INVALID_ARG;
+  const int64_t lim = int64_t(1) << 30;
+  if (B > lim || H > lim || q->size[2] > lim || Sk > lim || B * H > lim)
+    return SDPA_ERR_UNSUPPORTED;
+  return SDPA_OK;
+}
+
+sdpa_status check_common(double p, float scale) {
+  if (!(p >= 0.0 && p < 1.0)) return SDPA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return SDPA_ERR_INVALID_ARG;
+  return SDPA_OK;
+}
+
+// 4-D tensor map over the logical dims (D, S, H, B), 128-byte swizzle,
+// box = 64 elements (128 bytes) x box_rows rows.
+bool make_map(CUtensorMap* m, const sdpa_tensor* t, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(t->size[3]), static_cast<cuuint64_t>(t->size[2]),
+                        static_cast<cuuint64_t>(t->size[1]), static_cast<cuuint64_t>(t->size[0])};
+  cuuint64_t strides[3];
+  const int logical[3] = {2, 1, 0};  // S, H, B
+  for (int k = 0; k < 3; ++k) {
+    const int d = logical[k];
+    int64_t sbytes = t->stride[d] * 2;
+    if (t->size[d] <= 1) sbytes = 16;  // unused extent: any valid stride
+    strides[k] = static_cast<cuuint64_t>(sbytes);
+  }
+  cuuint32_t box[4] = {64, box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+PhiloxKey philox_key(uint64_t seed, uint64_t offset) {
+  PhiloxKey k;
+  k.k0 = static_cast<uint32_t>(seed);
+  k.k1 = static_cast<uint32_t>(seed >> 32);
+  k.off_lo = static_cast<uint32_t>(offset);
+  k.off_hi = static_cast<uint32_t>(offset >> 32);
+  return k;
+}
+
+uint32_t drop_threshold(double p) {
+  const double t = std::floor(p * 4294967296.0);
+  return t >= 4294967295.0 ? 0xFFFFFFFFu : static_cast<uint32_t>(t);
+}
+
+StridedBf16 strided(const sdpa_tensor* t) {
+  return StridedBf16{t->data, t->stride[0], t->stride[1], t->stride[2]};
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+sdpa_status finish(cudaError_t e, cudaStream_t stream) {
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  if (debug_sync()) return sdpa_check_device(reinterpret_cast<sdpa_stream_t>(stream));
+  return SDPA_OK;
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                     double dropout_p, int is_causal, float scale, uint64_t seed,
+                     uint64_t offset, sdpa_tensor* out, float* lse, sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  sdpa_status s = check_dims(q, k, v);
+  if (s != SDPA_OK) return s;
+  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
+  const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
+  if (D != 64 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(out, B, H, Sq, D)) != SDPA_OK) return s;
+  if (B * H * Sq == 0) return SDPA_OK;
+  if (Sk == 0) return SDPA_ERR_INVALID_ARG;  // softmax over no keys
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
+      !make_map(&maps[3], out, 128))
+    return SDPA_ERR_CUDA;
+  FwdParams p;
+  p.B = static_cast<int>(B);
+  p.H = static_cast<int>(H);
+  p.Sq = static_cast<int>(Sq);
+  p.Sk = static_cast<int>(Sk);
+  p.n_q_tiles = static_cast<int>((Sq + 127) / 128);
+  p.scale_log2 = scale * kLog2e;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
+  p.pk = philox_key(seed, offset);
+  p.lse = lse;
+  p.err = error_word();
+  p.wait_limit_ns = wait_limit_ns();
+  if (!p.err) return SDPA_ERR_CUDA;
+  const bool dropout = dropout_p > 0.0;
+  return finish(launch_fwd(static_cast<int>(D), is_causal != 0, dropout, maps, p, stream), stream);
+}
+
+size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D) {
+  (void)Sk;
+  if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
+  const int64_t Sq_pad = round_up(Sq, 128);
+  return static_cast<size_t>(B * H * Sq_pad * (D + 2) * 4);
+}
+
+sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                     const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                     double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                     float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                     void* workspace, size_t workspace_bytes, sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  sdpa_status s = check_dims(q, k, v);
+  if (s != SDPA_OK) return s;
+  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
+  const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
+  if (D != 64 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dout, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(out, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dq, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dk, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dv, B, H, Sk, D)) != SDPA_OK) return s;
+  if (B * H == 0) return SDPA_OK;
+  if (Sq == 0) {
+    // no queries: the key and value gradients are zero
+    cudaError_t e = launch_zero_fill(strided(dk), B, H, Sk, D, stream);
+    if (e == cudaSuccess) e = launch_zero_fill(strided(dv), B, H, Sk, D, stream);
+    return finish(e, stream);
+  }
+  if (Sk == 0) return SDPA_ERR_INVALID_ARG;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+  const size_t need = sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SDPA_ERR_WORKSPACE;
+
+  const int64_t Sq_pad = round_up(Sq, 128);
+  float* dq_acc = static_cast<float*>(workspace);
+  float* lse2 = dq_acc + B * H * Sq_pad * D;
+  float* delta = lse2 + B * H * Sq_pad;
+
+  const uint32_t mq = static_cast<uint32_t>(8192 / D);
+  CUtensorMap maps[6];
+  if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
+      !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
+    return SDPA_ERR_CUDA;
+
+  uint32_t* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+
+  PreParams pp;
+  pp.B = static_cast<int>(B);
+  pp.H = static_cast<int>(H);
+  pp.Sq = static_cast<int>(Sq);
+  pp.Sq_pad = static_cast<int>(Sq_pad);
+  pp.D = static_cast<int>(D);
+  pp.out = strided(out);
+  pp.dout = strided(dout);
+  pp.lse = lse;
+  pp.lse2 = lse2;
+  pp.delta = delta;
+  pp.dq_acc = dq_acc;
+  cudaError_t e = launch_bwd_preprocess(pp, stream);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+
+  BwdParams p;
+  p.B = pp.B;
+  p.H = pp.H;
+  p.Sq = pp.Sq;
+  p.Sk = static_cast<int>(Sk);
+  p.Sq_pad = pp.Sq_pad;
+  p.n_kv_tiles = static_cast<int>((Sk + 127) / 128);
+  p.scale_log2 = scale * kLog2e;
+  p.scale = scale;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
+  p.pk = philox_key(seed, offset);
+  p.dq_acc = dq_acc;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.err = err;
+  p.wait_limit_ns = wait_limit_ns();
+  e = launch_bwd_main(static_cast<int>(D), is_causal != 0, dropout_p > 0.0, maps, p, stream);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+
+  ConvParams cp;
+  cp.B = pp.B;
+  cp.H = pp.H;
+  cp.Sq = pp.Sq;
+  cp.Sq_pad = pp.Sq_pad;
+  cp.D = pp.D;
+  cp.scale = scale;
+  cp.dq_acc = dq_acc;
+  cp.dq = strided(dq);
+  return finish(launch_bwd_dq_convert(cp, stream), stream);
+}
+
+sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                    double dropout_p, uint64_t seed, uint64_t offset,
+                                    uint8_t* mask, sdpa_stream_t stream_) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return SDPA_ERR_INVALID_ARG;
+  if (!(dropout_p >= 0.0 && dropout_p < 1.0)) return SDPA_ERR_INVALID_ARG;
+  const int64_t total = B * H * Sq * Sk;
+  if (total == 0) return SDPA_OK;
+  if (!mask) return SDPA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int64_t blocks = (total + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(blocks > 152 * 32 ? 152 * 32 : blocks);
+  dropout_mask_kernel<<<grid, 256, 0, stream>>>(total, drop_threshold(dropout_p),
+                                                philox_key(seed, offset), mask);
+  return finish(cudaGetLastError(), stream);
+}
+
+sdpa_status sdpa_check_device(sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SDPA_ERR_CUDA;
+  uint32_t* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  uint32_t host = 0;
+  if (cudaMemcpy(&host, err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (host != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    return SDPA_ERR_DEVICE_TIMEOUT;
+  }
+  return SDPA_OK;
+}
+
+sdpa_status sdpa_selftest_wait_timeout(uint64_t limit_ns, sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint32_t* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  if (limit_ns == 0 || limit_ns > 10ull * 1000 * 1000 * 1000) return SDPA_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+  if (cudaGetLastError() != cudaSuccess) return SDPA_ERR_CUDA;
+  return sdpa_check_device(stream_);
+}
+
+const char* sdpa_status_string(sdpa_status status) {
+  switch (status) {
+    case SDPA_OK: return "SDPA_OK";
+    case SDPA_ERR_INVALID_ARG: return "SDPA_ERR_INVALID_ARG: invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported shape or layout (D must be 64 or 128, innermost)";
+    case SDPA_ERR_ALIGNMENT: return "SDPA_ERR_ALIGNMENT: base pointers and strides must be 16-byte aligned";
+    case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA: CUDA launch or driver call failed";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "SDPA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
+    case SDPA_ERR_WORKSPACE: return "SDPA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+  }
+  return "SDPA_ERR_UNKNOWN";
+}
+
+}  // extern "C"

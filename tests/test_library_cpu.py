@@ -1,0 +1,154 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library is built (nvcc cross-compiles sm_103a here), loaded, and every
+entry point declared in include/sdpa.h must be exported. Argument checks
+run entirely on the host before any CUDA call, so their status codes are
+tested here with fake pointers that are never dereferenced.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from scaled_dot_product_07_gb300 import _build
+    _build.build()
+    import scaled_dot_product_07_gb300 as sdpa
+    return sdpa.load_library()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "sdpa.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(sdpa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_dropout_mask_debug",
+              "sdpa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    names = declared_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/sdpa.h but not exported"
+    assert set(names) == set(sdpa.EXPORTED_SYMBOLS)
+
+
+def test_status_strings(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    for code, name in sdpa.STATUS_NAMES.items():
+        assert sdpa.sdpa_status_string(code).startswith(name)
+    assert "UNKNOWN" in sdpa.sdpa_status_string(99)
+
+
+def test_workspace_size(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    # fp32 dQ accumulator + two fp32 row vectors, Sq rounded up to 128
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (64 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(8, 16, 4096, 4096, 128) == 8 * 16 * 4096 * 130 * 4
+    assert sdpa.sdpa_bwd_workspace_size(0, 3, 200, 77, 64) == 0
+    assert sdpa.sdpa_bwd_workspace_size(1, 1, 0, 77, 64) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
+
+
+def desc(B, H, S, D, layout="BHSE", data=FAKE, stride=None):
+    import scaled_dot_product_07_gb300 as sdpa
+    t = sdpa.SdpaTensor()
+    t.data = data
+    for i, s in enumerate((B, H, S, D)):
+        t.size[i] = s
+    if stride is None:
+        stride = (H * S * D, S * D, D, 1) if layout == "BHSE" else (S * H * D, D, H * D, 1)
+    for i, s in enumerate(stride):
+        t.stride[i] = s
+    return t
+
+
+def fwd_status(lib, q, k, v, o, p=0.0, causal=0, scale=0.125, lse=FAKE):
+    r = ctypes.byref
+    return lib.sdpa_fwd(r(q), r(k), r(v), p, causal, scale, 1, 0, r(o), ctypes.c_void_p(lse), None)
+
+
+def test_forward_argument_errors(lib):
+    B, H, S, D = 2, 3, 100, 64
+    ok = lambda: desc(B, H, S, D)
+    assert fwd_status(lib, desc(B, H, S, 96), desc(B, H, S, 96), desc(B, H, S, 96), desc(B, H, S, 96)) == 2
+    # E != Ev
+    assert fwd_status(lib, ok(), ok(), desc(B, H, S, 128), ok()) == 1
+    # K and V disagree on Sk; batch mismatch
+    assert fwd_status(lib, ok(), ok(), desc(B, H, S + 1, D), ok()) == 1
+    assert fwd_status(lib, ok(), desc(B + 1, H, S, D), desc(B + 1, H, S, D), ok()) == 1
+    # out shape
+    assert fwd_status(lib, ok(), ok(), ok(), desc(B, H, S + 1, D)) == 1
+    # dropout probability and scale
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), p=1.0) == 1
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), p=-0.1) == 1
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), scale=0.0) == 1
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), scale=float("nan")) == 1
+    # D not innermost
+    assert fwd_status(lib, desc(B, H, S, D, stride=(H * S * D, S * D, 1, S)), ok(), ok(), ok()) == 2
+    # misaligned base pointer, misaligned stride
+    assert fwd_status(lib, desc(B, H, S, D, data=FAKE + 2), ok(), ok(), ok()) == 3
+    assert fwd_status(lib, desc(B, H, S, D, stride=(H * S * 72, S * 72, 68, 1)), ok(), ok(), ok()) == 3
+    # null data, null / misaligned lse
+    assert fwd_status(lib, desc(B, H, S, D, data=None), ok(), ok(), ok()) == 1
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), lse=0) == 1
+    assert fwd_status(lib, ok(), ok(), ok(), ok(), lse=FAKE + 2) == 1
+    # a key length of zero with queries present
+    assert fwd_status(lib, ok(), desc(B, H, 0, D), desc(B, H, 0, D), ok()) == 1
+
+
+def test_empty_problems_are_no_ops(lib):
+    D = 64
+    # Sq == 0 and B == 0 succeed without touching the device (no GPU here)
+    assert fwd_status(lib, desc(2, 3, 0, D), desc(2, 3, 5, D), desc(2, 3, 5, D), desc(2, 3, 0, D)) == 0
+    assert fwd_status(lib, desc(0, 3, 9, D), desc(0, 3, 5, D), desc(0, 3, 5, D), desc(0, 3, 9, D)) == 0
+    r = ctypes.byref
+    z = desc(0, 2, 4, D)
+    assert lib.sdpa_bwd(r(z), r(z), r(z), r(z), r(z), None, 0.0, 0, 0, 0, 0.125, r(z), r(z), r(z),
+                        None, 0, None) == 0
+    assert lib.sdpa_dropout_mask_debug(0, 2, 3, 4, 0.1, 1, 2, None, None) == 0
+
+
+def test_backward_argument_errors(lib):
+    B, H, Sq, Sk, D = 1, 2, 100, 70, 128
+    q, kk = desc(B, H, Sq, D), desc(B, H, Sk, D)
+    r = ctypes.byref
+
+    def st(ws=FAKE, ws_bytes=1 << 30, dk=None, p=0.0):
+        return lib.sdpa_bwd(r(q), r(q), r(kk), r(kk), r(q), ctypes.c_void_p(FAKE), p, 1, 0, 0,
+                            0.1, r(q), r(dk or kk), r(kk), ctypes.c_void_p(ws), ws_bytes, None)
+
+    need = lib.sdpa_bwd_workspace_size(B, H, Sq, Sk, D)
+    assert st(ws=0) == 6
+    assert st(ws_bytes=need - 1) == 6
+    assert st(ws=FAKE + 16) == 6  # workspace must be 256-byte aligned
+    assert st(dk=desc(B, H, Sk + 1, D)) == 1
+    assert st(p=1.5) == 1
+
+
+def test_mask_debug_argument_errors(lib):
+    assert lib.sdpa_dropout_mask_debug(1, 1, 4, 4, 1.0, 0, 0, ctypes.c_void_p(FAKE), None) == 1
+    assert lib.sdpa_dropout_mask_debug(1, 1, 4, 4, 0.5, 0, 0, None, None) == 1
+    assert lib.sdpa_dropout_mask_debug(-1, 1, 4, 4, 0.5, 0, 0, ctypes.c_void_p(FAKE), None) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import scaled_dot_product_07_gb300 as sdpa
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        sdpa.sdpa_fwd(x, x, x)
