@@ -311,35 +311,39 @@ def bench_ours(args, w):
     peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
     # ---- end to end through the public API with host buffers
-    pin = lambda t: t.pin_memory()
-    hq, hk, hv, hdo = (pin(x) for x in inputs_cpu)
-    hout, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, q, k, v))
-    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
-    d2h = sum(x.numel() * x.element_size() for x in (hout, hlse, hdq, hdk, hdv))
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()
+        hq, hk, hv, hdo = (pin(x) for x in inputs_cpu)
+        hout, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, q, k, v))
+        hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (hout, hlse, hdq, hdk, hdv))
 
-    def e2e_step():
-        dq_, dk_, dv_ = (x.to(dev, non_blocking=True) for x in (hq, hk, hv))
-        ddo = hdo.to(dev, non_blocking=True)
-        o, l, s_, off_ = sdpa.sdpa_fwd(dq_, dk_, dv_, w.dropout_p, w.is_causal, None, w.seed, w.offset)
-        g = sdpa.sdpa_bwd(ddo, dq_, dk_, dv_, o, l, w.dropout_p, w.is_causal, s_, off_, None)
-        for src, dst in zip((o, l) + g, (hout, hlse, hdq, hdk, hdv)):
-            dst.copy_(src, non_blocking=True)
+        def e2e_step():
+            dq_, dk_, dv_ = (x.to(dev, non_blocking=True) for x in (hq, hk, hv))
+            ddo = hdo.to(dev, non_blocking=True)
+            o, l, s_, off_ = sdpa.sdpa_fwd(dq_, dk_, dv_, w.dropout_p, w.is_causal, None, w.seed,
+                                           w.offset)
+            g = sdpa.sdpa_bwd(ddo, dq_, dk_, dv_, o, l, w.dropout_p, w.is_causal, s_, off_, None)
+            for src, dst in zip((o, l) + g, (hout, hlse, hdq, hdk, hdv)):
+                dst.copy_(src, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 10))
-    e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+        e2e_steps = max(3, min(args.steps, 10))
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = barrier_max(e0.elapsed_time(e1), world) / e2e_steps
-    e2e_val = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = barrier_max(e0.elapsed_time(e1), world) / e2e_steps
+        e2e = {"value": world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     if rank != 0:
         return 0
@@ -367,8 +371,7 @@ def bench_ours(args, w):
                          "unit": "TFLOP/s", "frac": fwd_tf / peak,
                          "traffic": kernel_traffic("fwd_kernel"),
                          "peak_source": f"{pk_src} bf16_tflops (burst)"},
-        "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -385,9 +388,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (small cases for profiling; not a bench line)")
     args = ap.parse_args()
     from scaled_dot_product_07_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD]
+    if args.batch is not None:
+        w = W.make_workload(WORKLOAD, B=args.batch)
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_ours(args, w)
