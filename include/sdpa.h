@@ -114,6 +114,39 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
                      float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
                      void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
 
+/* Size of the scratch array built into the library for sdpa_bwd_noalloc. */
+#define SDPA_BWD_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * sdpa_bwd_noalloc — the same backward as sdpa_bwd, for callers that cannot
+ * allocate device memory: code that a host framework hands only its input
+ * and output buffers, under rules that forbid private cudaMalloc calls
+ * (they would bypass the framework's memory pool and accounting), and
+ * latency-critical loops where an allocation, which may synchronise the
+ * device, is not acceptable. The pages have no counterpart; this is a
+ * convenience of this library.
+ *   Arguments are those of sdpa_bwd without the workspace; the caller still
+ *   passes every input and output. The workspace comes from one fixed array
+ *   of SDPA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library:
+ *   every GPU that loads the library holds it until the process exits.
+ *   Problems whose sdpa_bwd_workspace_size() exceeds that maximum are
+ *   rejected with SDPA_ERR_WORKSPACE and nothing is launched.
+ *   Nothing is allocated: no cudaMalloc or cudaFree, no allocating library
+ *   routine. The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   All calls share the one array, which keeps whatever the last call left
+ *   in it (every call overwrites what it reads, so results do not depend on
+ *   it). Calls whose work overlaps on the GPU -- e.g. issued to two streams
+ *   without ordering between them -- race on the array and give wrong
+ *   results; order them on one stream.
+ */
+sdpa_status sdpa_bwd_noalloc(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                             const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                             double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                             float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                             sdpa_stream_t stream);
+
 /*
  * sdpa_dropout_mask_debug — writes the keep mask (1 = kept, 0 = dropped) of
  * every element of a [B,H,Sq,Sk] attention problem into `mask` (uint8, device,

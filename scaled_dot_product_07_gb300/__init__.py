@@ -25,6 +25,7 @@ __all__ = [
     "SdpaError", "load_library", "library_path", "sdpa_fwd", "sdpa_bwd",
     "sdpa_bwd_workspace_size", "sdpa_dropout_mask_debug", "sdpa_check_device",
     "sdpa_selftest_wait_timeout", "sdpa_status_string", "SDPAFunction", "EXPORTED_SYMBOLS",
+    "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,8 +35,11 @@ _LIB = None
 # Every entry point of include/sdpa.h.
 EXPORTED_SYMBOLS = (
     "sdpa_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_dropout_mask_debug",
-    "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string",
+    "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string", "sdpa_bwd_noalloc",
 )
+
+# SDPA_BWD_NOALLOC_SCRATCH_BYTES of include/sdpa.h
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 SDPA_OK = 0
 STATUS_NAMES = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
@@ -80,6 +84,9 @@ def load_library(path=None):
     lib.sdpa_bwd.argtypes = [P, P, P, P, P, vp, dbl, ctypes.c_int, u64, u64, flt, P, P, P, vp,
                              ctypes.c_size_t, vp]
     lib.sdpa_bwd.restype = ctypes.c_int
+    lib.sdpa_bwd_noalloc.argtypes = [P, P, P, P, P, vp, dbl, ctypes.c_int, u64, u64, flt, P, P, P,
+                                     vp]
+    lib.sdpa_bwd_noalloc.restype = ctypes.c_int
     lib.sdpa_dropout_mask_debug.argtypes = [i64, i64, i64, i64, dbl, u64, u64, vp, vp]
     lib.sdpa_dropout_mask_debug.restype = ctypes.c_int
     lib.sdpa_check_device.argtypes = [vp]
@@ -189,6 +196,33 @@ def sdpa_bwd(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, of
                       ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                       _stream(q.device))
     _check(st, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def sdpa_bwd_noalloc(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
+                     scale=None, dq=None, dk=None, dv=None):
+    """Backward without a caller workspace: the library's built-in scratch
+    array (NOALLOC_SCRATCH_BYTES) is used instead. For callers that may not
+    allocate device memory; the output tensors must still be provided (or
+    are allocated here by torch when omitted, for convenience in Python).
+    Calls that overlap on the GPU share the scratch and race; keep them on
+    one stream."""
+    import torch
+    lib = load_library()
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_tensor(t, n)
+    D = q.shape[3]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    descs = [_desc(t) for t in (dout, q, k, v, out, dq, dk, dv)]
+    refs = [ctypes.byref(d) for d in descs]
+    st = lib.sdpa_bwd_noalloc(refs[0], refs[1], refs[2], refs[3], refs[4],
+                              ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                              float(dropout_p), int(bool(is_causal)), int(seed), int(offset),
+                              _default_scale(D, scale), refs[5], refs[6], refs[7],
+                              _stream(q.device))
+    _check(st, "sdpa_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -152,3 +152,14 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         sdpa.sdpa_fwd(x, x, x)
+
+
+def test_noalloc_backward_rejects_oversize_problems_on_the_host(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    B, H, S, D = 8, 16, 4096, 128
+    assert lib.sdpa_bwd_workspace_size(B, H, S, S, D) > sdpa.NOALLOC_SCRATCH_BYTES
+    t = desc(B, H, S, D)
+    r = ctypes.byref
+    st = lib.sdpa_bwd_noalloc(r(t), r(t), r(t), r(t), r(t), ctypes.c_void_p(FAKE), 0.0, 1, 0, 0,
+                              0.1, r(t), r(t), r(t), None)
+    assert st == 6
