@@ -27,7 +27,7 @@ enum WaitSite : uint32_t {
 
 struct FwdParams {
   int B, H, Sq, Sk;
-  int n_q_tiles;          // ceil(Sq / 128)
+  int n_q_tiles;          // ceil(Sq / 256): pairs of 128-row query tiles per head
   float scale_log2;       // softmax scale * log2(e)
   uint32_t drop_threshold;  // floor(p * 2^32)
   float drop_rescale;       // 1 / (1 - p)

@@ -216,7 +216,7 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
   p.H = static_cast<int>(H);
   p.Sq = static_cast<int>(Sq);
   p.Sk = static_cast<int>(Sk);
-  p.n_q_tiles = static_cast<int>((Sq + 127) / 128);
+  p.n_q_tiles = static_cast<int>((Sq + 255) / 256);  // pairs of 128-row query tiles
   p.scale_log2 = scale * kLog2e;
   p.drop_threshold = drop_threshold(dropout_p);
   p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));

@@ -230,9 +230,11 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int kv_tile = blockIdx.x / BH;  // low key tiles (most causal work) first
-  const int bh = blockIdx.x - kv_tile * BH;
+  // head-major order: the CTAs of one head run together, so the head's Q and
+  // dO tiles (which every one of them streams) stay in L2; within a head the
+  // low key tiles (the most causal work) go first
+  const int bh = blockIdx.x / p.n_kv_tiles;
+  const int kv_tile = blockIdx.x - bh * p.n_kv_tiles;
   const int b = bh / p.H;
   const int h = bh - b * p.H;
   const int k0 = kv_tile * 128;

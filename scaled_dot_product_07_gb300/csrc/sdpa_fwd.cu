@@ -4,20 +4,30 @@
 // natural-log log-sum-exp of each score row, stashed for the backward
 // (NVIDIA/Fuser issue 2278, "SdpaOpFwd / SdpaOpBwd nodes").
 //
-// One CTA computes one 128-row query tile of one (batch, head):
-//   warp 4      TMA producer: Q once, then K_j and V_j through a ring of
-//               shared-memory stages (128-byte swizzled, 64-column slabs).
-//   warp 5      TMEM allocator and MMA issuer (one thread): S_j = Q K_j^T
-//               into one of two TMEM score buffers, then O += P_{j-1} V_{j-1}
-//               so the tensor core computes the next scores while the
-//               softmax warps work on the current ones.
-//   warps 0-3   softmax: thread r owns query row r. It reads its score row
-//               from TMEM, applies the causal / key-tail mask, keeps the
-//               running row max m (base-2, scaled) and sum l, rescales the
-//               O row in TMEM only when the max grew by more than 2^8,
-//               writes P (bf16, dropout applied) to shared memory for the
-//               P V product, and at the end writes out = O / l (TMA store)
-//               and lse = (m + log2 l) * ln 2.
+// One CTA computes two 128-row query tiles (Q0, Q1: 256 rows) of one
+// (batch, head), 320 threads:
+//   warp 9      TMA producer: Q0, Q1 once, then K_j and V_j (separate
+//               barriers) through a ring of 128-byte-swizzled stages.
+//   warp 8      TMEM allocator and MMA issuer (one thread). TMEM holds
+//               S0, S1 (128 fp32 columns each) and O0, O1 (D columns each).
+//               Per key tile j it issues, in this order,
+//                 O0 += P0_j V_j,  S0_{j+1} = Q0 K_{j+1}^T,
+//                 O1 += P1_j V_j,  S1_{j+1} = Q1 K_{j+1}^T,
+//               so that while one softmax warpgroup works on its scores the
+//               tensor core runs the other tile's products (ping-pong).
+//               P_i is bf16 written by the softmax into the first 64 columns
+//               of S_i and is read straight from TMEM as the A operand.
+//   warps 0-3   softmax of Q0, warps 4-7 softmax of Q1: thread r owns query
+//               row r of its tile. Per key tile it loads the score row, masks
+//               the causal diagonal / key tail, keeps the running row max m
+//               and sum l, rescales its O row in TMEM only when the max grew
+//               by more than 2^8 (exact: the shift only changes the common
+//               reference), and stores P (bf16, dropout applied) into TMEM.
+//               At the end it writes out = O / l (TMA store through shared
+//               memory) and lse = m * scale + ln l.
+// The completion of S_i(j+1) implies that O_i += P_i(j) V_j has completed
+// (tcgen05 operations of one issuing thread complete in order), so the
+// softmax may touch O_i as soon as it sees its next scores.
 // Key tiles entirely above the causal diagonal are never loaded or computed.
 #include "common.cuh"
 
@@ -29,18 +39,20 @@ struct FwdLayout {
   static constexpr int kSlabBytes = 128 * 128;            // 128 rows x 128 bytes
   static constexpr int kTileBytes = 128 * D * 2;          // 128 rows x D bf16
   static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQ = 0;                            // Q0, Q1
+  static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;     // 128 x 128 bf16, 2 slabs
-  static constexpr int kBar = kP + 2 * kSlabBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], p_full, o_done, fin
-  static constexpr int kNumBars = 1 + 2 * kStages + 2 + 2 + 3;
+  static constexpr int kBar = kV + kStages * kTileBytes;
+  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2]
+  static constexpr int kNumBars = 1 + 3 * kStages + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;             // room to align to 1024
   // TMEM columns
-  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO = 256, kTmemCols = 512;
+  __host__ __device__ static constexpr uint32_t tmem_s(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t tmem_o(int i) { return 256u + D * i; }
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 320;
 };
 
 __device__ __forceinline__ void reg_touch(uint32_t (&r)[32]) {
@@ -53,8 +65,16 @@ __device__ __forceinline__ void reg_touch(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
+// Number of key tiles that query rows [r0, r0+128) ∩ [0, Sq) can see.
+__device__ __forceinline__ int kv_tiles_for(int r0, int Sq, int Sk, bool causal) {
+  if (r0 >= Sq) return 0;
+  const int n = (Sk + 127) / 128;
+  if (!causal) return n;
+  return min(n, min(r0 + 127, Sq - 1) / 128 + 1);
+}
+
 template <int D, bool CAUSAL, bool DROPOUT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const FwdParams p) {
@@ -67,46 +87,47 @@ __global__ void __launch_bounds__(192, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + S;
-  uint64_t* s_full = kv_empty + S;
-  uint64_t* s_empty = s_full + 2;
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* fin = o_done + 1;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + S;
+  uint64_t* kv_empty = v_full + S;
+  uint64_t* s_full = kv_empty + S;   // [2]
+  uint64_t* p_full = s_full + 2;     // [2]
+  uint64_t* o_full = p_full + 2;     // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int BH = p.B * p.H;
-  int q_tile = blockIdx.x / BH;
-  const int bh = blockIdx.x - q_tile * BH;
-  if (CAUSAL) q_tile = p.n_q_tiles - 1 - q_tile;  // longest tiles first
+  // head-major order (a head's K/V stays in L2 while its tiles run);
+  // within a head the longest causal tiles go first
+  const int n_pairs = p.n_q_tiles;  // tile pairs per head
+  const int bh = blockIdx.x / n_pairs;
+  int pair = blockIdx.x - bh * n_pairs;
+  if (CAUSAL) pair = n_pairs - 1 - pair;
   const int b = bh / p.H;
   const int h = bh - b * p.H;
-  const int q0 = q_tile * 128;
-  int n_kv = (p.Sk + 127) / 128;
-  if (CAUSAL) n_kv = min(n_kv, min(q0 + 127, p.Sq - 1) / 128 + 1);
+  const int q0 = pair * 256;
+  const int n_t[2] = {kv_tiles_for(q0, p.Sq, p.Sk, CAUSAL),
+                      kv_tiles_for(q0 + 128, p.Sq, p.Sk, CAUSAL)};
+  const int n_kv = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_full[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
-    mbar_init(fin, 1);
     *abort_word = 0u;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 8) {
     tmem_alloc(tmem_holder, L::kTmemCols);
     tmem_relinquish();
   }
@@ -116,222 +137,234 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl wc{abort_word, p.err, p.wait_limit_ns};
 
-  if (warp == 4) {
+  if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(q_full, L::kTileBytes);
+      const int nq = n_t[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+      for (int i = 0; i < nq; ++i) {
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        tma_load_4d(smem + L::kQ + s * L::kSlabBytes, &tm_q, q_full, s * 64, q0, h, b);
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, &tm_q, q_full, s * 64,
+                      q0 + 128 * i, h, b);
+      }
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
         if (j >= S) mbar_wait(&kv_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * L::kTileBytes);
+        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s) {
-          tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &kv_full[st],
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
                       s * 64, j * 128, h, b);
-          tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &kv_full[st],
+        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &v_full[st],
                       s * 64, j * 128, h, b);
-        }
       }
       if (*abort_word) {
         // give the loads still in flight time to land before the CTA exits
-        for (int j = max(0, n_kv - S); j < n_kv; ++j)
-          mbar_wait_drain(&kv_full[j % S], (j / S) & 1, 2000000ull);
+        for (int j = max(0, n_kv - S); j < n_kv; ++j) {
+          mbar_wait_drain(&k_full[j % S], (j / S) & 1, 2000000ull);
+          mbar_wait_drain(&v_full[j % S], (j / S) & 1, 2000000ull);
+        }
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t tS[2] = {tmem + L::kTmemS0, tmem + L::kTmemS1};
-      const uint32_t tO = tmem + L::kTmemO;
+      auto issue_s = [&](int i, int j) {
+        const int st = j % S;
+        const uint32_t qa = sb + L::kQ + i * L::kTileBytes;
+        const uint32_t ka = sb + L::kK + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + L::tmem_s(i), sdesc_sw128(qa + koff, 16, 1024),
+                      sdesc_sw128(ka + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[i]);
+      };
+      auto issue_pv = [&](int i, int j) {
+        const int st = j % S;
+        const uint32_t va = sb + L::kV + st * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + kk * 8,
+                      sdesc_sw128(va + kk * 2048, L::kSlabBytes, 1024), kIdO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      };
       mbar_wait(q_full, 0, wc, kSiteFwdQFull);
-      for (int j = 0; j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int st = j % S;
-          const int sbuf = j & 1;
-          mbar_wait(&kv_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
-          if (j >= 2) mbar_wait(&s_empty[sbuf], ((j >> 1) - 1) & 1, wc, kSiteFwdSEmpty);
-          tc_fence_after();
-          const uint32_t qa = sb + L::kQ;
-          const uint32_t ka = sb + L::kK + st * L::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
-            mma_bf16_ss(tS[sbuf], sdesc_sw128(qa + koff, 16, 1024),
-                        sdesc_sw128(ka + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(&s_full[sbuf]);
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % S;
-          mbar_wait(p_full, jj & 1, wc, kSiteFwdPFull);
-          tc_fence_after();
-          const uint32_t pa = sb + L::kP;
-          const uint32_t va = sb + L::kV + st * L::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t poff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
-            mma_bf16_ss(tO, sdesc_sw128(pa + poff, 16, 1024),
-                        sdesc_sw128(va + kk * 2048, L::kSlabBytes, 1024), kIdO,
-                        (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(o_done);
-          mma_commit(&kv_empty[st]);
-        }
+      if (n_kv > 0) {
+        mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+        tc_fence_after();
+        for (int i = 0; i < 2; ++i)
+          if (n_t[i] > 0) issue_s(i, 0);
       }
-      // every MMA must be complete before the TMEM is released
-      mma_commit(fin);
-      mbar_wait_drain(fin, 0, 2000000000ull);
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % S;
+        mbar_wait(&v_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
+        for (int i = 0; i < 2; ++i) {
+          if (j >= n_t[i]) continue;
+          mbar_wait(&p_full[i], j & 1, wc, kSiteFwdPFull);
+          tc_fence_after();
+          issue_pv(i, j);
+          if (j + 1 < n_t[i]) {
+            const int st1 = (j + 1) % S;
+            mbar_wait(&k_full[st1], ((j + 1) / S) & 1, wc, kSiteFwdKvFull);
+            tc_fence_after();
+            issue_s(i, j + 1);
+          } else {
+            mma_commit(&o_full[i]);
+          }
+        }
+        mma_commit(&kv_empty[st]);
+      }
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warps 0-3
-    const int row = threadIdx.x;  // query row within the tile == TMEM lane
-    const int qi = q0 + row;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS[2] = {tmem + L::kTmemS0 + lane_base, tmem + L::kTmemS1 + lane_base};
-    const uint32_t tO = tmem + L::kTmemO + lane_base;
+    // ------------------------------------------------------------ softmax warpgroups
+    const int i = warp >> 2;          // query tile of this warpgroup
+    const int row = threadIdx.x & 127;  // row in the tile == TMEM lane
+    const int qi = q0 + 128 * i + row;
+    const int n_mine = n_t[i];
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
+    const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
     const uint64_t n_row = (static_cast<uint64_t>(bh) * p.Sq + qi) * static_cast<uint64_t>(p.Sk);
-    float m = -INFINITY;
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of the raw scores of this row
     float l = 0.f;
 
-    for (int j = 0; j < n_kv; ++j) {
-      const int sbuf = j & 1;
-      mbar_wait(&s_full[sbuf], (j >> 1) & 1, wc, kSiteFwdSFull);
+    for (int j = 0; j < n_mine; ++j) {
+      mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS[sbuf] + 0, r0);
-      tmem_ld32(tS[sbuf] + 32, r1);
-      tmem_ld32(tS[sbuf] + 64, r2);
-      tmem_ld32(tS[sbuf] + 96, r3);
+      tmem_ld32(tS + 0, r0);
+      tmem_ld32(tS + 32, r1);
+      tmem_ld32(tS + 64, r2);
+      tmem_ld32(tS + 96, r3);
       tmem_ld_wait(r0);
       reg_touch(r1);
       reg_touch(r2);
       reg_touch(r3);
-      tc_fence_before();
-      mbar_arrive(&s_empty[sbuf]);
-
       float x[128];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(r0[i]) * p.scale_log2;
-        x[32 + i] = __uint_as_float(r1[i]) * p.scale_log2;
-        x[64 + i] = __uint_as_float(r2[i]) * p.scale_log2;
-        x[96 + i] = __uint_as_float(r3[i]) * p.scale_log2;
+      for (int c = 0; c < 32; ++c) {
+        x[c] = __uint_as_float(r0[c]);
+        x[32 + c] = __uint_as_float(r1[c]);
+        x[64 + c] = __uint_as_float(r2[c]);
+        x[96 + c] = __uint_as_float(r3[c]);
       }
       const int k0 = j * 128;
-      const bool tail = k0 + 128 > p.Sk;
-      const bool diag = CAUSAL && (k0 + 127 > q0);
-      if (tail || diag) {
+      if ((k0 + 128 > p.Sk) || (CAUSAL && k0 + 127 > q0 + 128 * i)) {
         const int lim = CAUSAL ? min(p.Sk - k0, qi - k0 + 1) : (p.Sk - k0);
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= lim) x[i] = -INFINITY;
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
       }
-      float mx = x[0];
+      float mx = fmaxf(x[0], x[1]);
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, x[i]);
+      for (int c = 2; c < 128; c += 2) mx = fmaxf(mx, fmaxf(x[c], x[c + 1]));
       const float m_new = fmaxf(m, mx);
-
-      if (j >= 1) {
-        // O and the P buffer are free once the previous P V product is done
-        mbar_wait(o_done, (j - 1) & 1, wc, kSiteFwdODone);
-        tc_fence_after();
-        const bool grow = m_new > m + 8.0f;
-        if (__any_sync(0xffffffffu, grow)) {
-          const float alpha = ex2_approx(m - m_new);
-          l *= alpha;
-          m = m_new;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
-          tmem_st_wait();
-        }
-      } else {
+      if (j == 0) {
         m = m_new;
+      } else if (__any_sync(0xffffffffu, (m_new - m) * sl2 > 8.0f)) {
+        // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
+        const float alpha = ex2_approx((m - m_new) * sl2);
+        l *= alpha;
+        m = m_new;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32, o);
+        }
       }
+      const float neg = -m * sl2;
 
       uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (DROPOUT) keep_bits_128(n_row + k0, p.drop_threshold, p.pk, keep);
-      float rs = 0.f;
-      uint32_t pk2[64];
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < 128; i += 2) {
-        float e0 = ex2_approx(x[i] - m);
-        float e1 = ex2_approx(x[i + 1] - m);
-        rs += e0 + e1;
-        if (DROPOUT) {
-          e0 = ((keep[i >> 5] >> (i & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
-          e1 = ((keep[(i + 1) >> 5] >> ((i + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk2[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const int e = hf * 64 + c;
+          float e0 = ex2_approx(fmaf(x[e], sl2, neg));
+          float e1 = ex2_approx(fmaf(x[e + 1], sl2, neg));
+          rs0 += e0;
+          rs1 += e1;
+          if (DROPOUT) {
+            e0 = ((keep[e >> 5] >> (e & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
+            e1 = ((keep[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
+          }
+          pk2[c >> 1] = pack_bf16x2(e0, e1);
         }
-        pk2[i >> 1] = pack_bf16x2(e0, e1);
+        // P columns [32 hf, 32 hf + 32) overwrite scores already held in registers
+        tmem_st32(tS + hf * 32, pk2);
       }
-      l += rs;
-      const uint32_t pa = sb + L::kP;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_shared_v4(pa + (c >> 3) * L::kSlabBytes + sw128_offset(row, c & 7), pk2[4 * c],
-                     pk2[4 * c + 1], pk2[4 * c + 2], pk2[4 * c + 3]);
-      fence_async_smem();
+      l += rs0 + rs1;
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[i]);
     }
 
     // ------------------------------------------------------------ epilogue
-    mbar_wait(o_done, (n_kv - 1) & 1, wc, kSiteFwdODone);
-    tc_fence_after();
-    const float inv_l = 1.f / l;
-    const uint32_t oa = sb + L::kQ;  // Q is dead: every MMA has completed
+    if (n_mine > 0) {
+      mbar_wait(&o_full[i], 0, wc, kSiteFwdODone);
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const uint32_t oa = sb + L::kQ + i * L::kTileBytes;  // Q_i is dead after o_full[i]
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(tO + c * 32, o);
-      tmem_ld_wait(o);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait(o);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int col0 = c * 32 + q4 * 8;
-        const uint32_t addr = oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3);
-        st_shared_v4(addr,
-                     pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
-                                 __uint_as_float(o[q4 * 8 + 1]) * inv_l),
-                     pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
-                                 __uint_as_float(o[q4 * 8 + 3]) * inv_l),
-                     pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
-                                 __uint_as_float(o[q4 * 8 + 5]) * inv_l),
-                     pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
-                                 __uint_as_float(o[q4 * 8 + 7]) * inv_l));
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col0 = c * 32 + q4 * 8;
+          const uint32_t addr =
+              oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3);
+          st_shared_v4(addr,
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
+                                   __uint_as_float(o[q4 * 8 + 1]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
+                                   __uint_as_float(o[q4 * 8 + 3]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
+                                   __uint_as_float(o[q4 * 8 + 5]) * inv_l),
+                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
+                                   __uint_as_float(o[q4 * 8 + 7]) * inv_l));
+        }
       }
-    }
-    if (qi < p.Sq) p.lse[static_cast<size_t>(bh) * p.Sq + qi] = (m + log2f(l)) * kLn2;
-    fence_async_smem();
-    named_barrier_sync(1, 128);
-    if (row == 0) {
+      if (qi < p.Sq)
+        p.lse[static_cast<size_t>(bh) * p.Sq + qi] = m * (sl2 * kLn2) + __logf(l);
+      fence_async_smem();
+      named_barrier_sync(1 + i, 128);
+      if (row == 0) {
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        tma_store_4d(&tm_o, smem + L::kQ + s * L::kSlabBytes, s * 64, q0, h, b);
-      bulk_commit();
-      bulk_wait_all();
+        for (int s = 0; s < D / 64; ++s)
+          tma_store_4d(&tm_o, smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, s * 64,
+                       q0 + 128 * i, h, b);
+        bulk_commit();
+        bulk_wait_all();
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmemCols);
   }
@@ -344,7 +377,7 @@ cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
-  kern<<<grid, 192, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
 
