@@ -81,6 +81,9 @@ cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout,
                             const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
                             cudaStream_t stream);
+cudaError_t launch_bwd_main_d128(bool causal, bool dropout,
+                                 const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
+                                 cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStream_t stream);
 cudaError_t launch_dropout_mask(int64_t B, int64_t H, int64_t Sq, int64_t Sk, uint32_t threshold,
@@ -90,6 +93,7 @@ cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t 
 // Dynamic shared memory sizes (for validation against the device limit).
 size_t fwd_smem_bytes(int D);
 size_t bwd_smem_bytes(int D);
+size_t bwd_d128_smem_bytes();
 
 __host__ __device__ inline uint8_t* align_up_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023u) &

@@ -9,7 +9,8 @@
 // Three kernels on one stream:
 //   bwd_preprocess_kernel  Delta_i = sum_e dO_ie * O_ie, lse * log2(e) into a
 //                          padded workspace (+inf past Sq), dQ accumulator := 0
-//   bwd_main_kernel        one CTA per 128-key tile of one (batch, head); it
+//   bwd_main_kernel        (head dim 64; head dim 128 has its own kernel in
+//                          sdpa_bwd128.cu) one CTA per 128-key tile of one (batch, head); it
 //                          walks the query tiles that can see its keys:
 //                            S^T  = K Q_i^T             (tcgen05, TMEM)
 //                            dP~^T = V dO_i^T           (tcgen05, TMEM)
@@ -586,7 +587,7 @@ unsigned elementwise_grid(int64_t work_items) {
 }  // namespace
 
 size_t bwd_smem_bytes(int D) {
-  return D == 64 ? BwdLayout<64>::kAlloc : BwdLayout<128>::kAlloc;
+  return D == 64 ? BwdLayout<64>::kAlloc : bwd_d128_smem_bytes();
 }
 
 cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream) {
@@ -616,11 +617,8 @@ cudaError_t launch_bwd_main(int D, bool causal, bool dropout, const CUtensorMap*
   SDPA_BWD_CASE(64, false, true)
   SDPA_BWD_CASE(64, true, false)
   SDPA_BWD_CASE(64, true, true)
-  SDPA_BWD_CASE(128, false, false)
-  SDPA_BWD_CASE(128, false, true)
-  SDPA_BWD_CASE(128, true, false)
-  SDPA_BWD_CASE(128, true, true)
 #undef SDPA_BWD_CASE
+  if (D == 128) return launch_bwd_main_d128(causal, dropout, maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,0 +1,469 @@
+// Main backward kernel for head dim 128 (sdpfa_bwd of test_sdpa_loop_split,
+// "DID loop split for SDPA", NVIDIA/Fuser PR 3711; probabilities recomputed
+// from the stashed log-sum-exp, NVIDIA/Fuser issue 2278; dropout mask
+// regenerated from the absolute index, "REDO of dropout support for mem eff
+// #102038").
+//
+// One CTA per 128-key tile of one (batch, head); it walks the 64-row query
+// steps that can see its keys. 448 threads:
+//   warp 13     TMA: K, V once; Q_t, dO_t, lse2_t, Delta_t through a 3-stage ring
+//   warp 12     TMEM allocator and MMA issuer (one thread)
+//   warps 0-3   compute warpgroup A (even steps), warps 4-7 B (odd steps):
+//               thread = key row. P^T = exp2(S^T*scale*log2e - lse2) (masked,
+//               dropout applied) is stored as bf16 into TMEM (A operand of
+//               dV += P~^T dO); dS^T = P^T (dP~^T keep/(1-p) - Delta) is
+//               stored as bf16 into shared memory (operand of dK and dQ).
+//   warps 8-11  dQ warpgroup: reads the dQ^T partial of a step from TMEM,
+//               stages it fp32 [64 x 128] and reduces it into the global fp32
+//               accumulator with one bulk reduce-add.
+// TMEM (512 columns): dV [0,128), dK [128,256), and two step buffers
+// {S^T, dP^T} at [256,384) and [384,512). A step's dQ^T partial (M = D =
+// 128 lanes, 64 columns) overwrites its own S^T columns once dV has read
+// P~^T from them (tcgen05 MMAs of one thread execute in order).
+// MMA order per step t: S^T(t), dP^T(t), then dV, dK, dQ of step t-1, so
+// the tensor core computes the next step's products while a compute
+// warpgroup works on the current one.
+#include "common.cuh"
+
+namespace sdpa {
+namespace {
+
+struct B128 {
+  static constexpr int D = 128;
+  static constexpr int kMq = 64;                 // query rows per step
+  static constexpr int kStages = 3;              // Q / dO ring
+  static constexpr int kKvSlab = 128 * 128;      // 128 rows x 128 bytes
+  static constexpr int kKvBytes = 128 * D * 2;   // 32 KB
+  static constexpr int kQSlab = kMq * 128;       // 8 KB
+  static constexpr int kQBytes = kMq * D * 2;    // 16 KB
+  static constexpr int kDsBytes = 128 * kMq * 2; // [128 keys x 64 q] bf16 = 16 KB
+  static constexpr int kDqBytes = kMq * D * 4;   // 32 KB fp32 staging
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kKvBytes;
+  static constexpr int kQ = kV + kKvBytes;
+  static constexpr int kDO = kQ + kStages * kQBytes;
+  static constexpr int kDs = kDO + kStages * kQBytes;        // [2]
+  static constexpr int kDq = kDs + 2 * kDsBytes;
+  static constexpr int kLse = kDq + kDqBytes;                // [kStages][64] fp32
+  static constexpr int kDelta = kLse + kStages * kMq * 4;    // [kStages][64] fp32
+  static constexpr int kBar = kDelta + kStages * kMq * 4;
+  // kv_full, q_full[S], q_empty[S], and per step buffer b in {0,1}:
+  // s_full, dp_full, p_full, ds_full, sp_empty, dq_full, dq_empty, ds_empty; done
+  static constexpr int kNumBars = 1 + 2 * kStages + 8 * 2 + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemCols = 512;
+  __host__ __device__ static constexpr uint32_t tmem_s(int b) { return 256u + 128u * b; }
+  __host__ __device__ static constexpr uint32_t tmem_dp(int b) { return 320u + 128u * b; }
+  static constexpr int kThreads = 448;
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void touch32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
+template <bool CAUSAL, bool DROPOUT>
+__global__ void __launch_bounds__(448, 1)
+    bwd_main_kernel_d128(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dk,
+                         const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
+  using L = B128;
+  constexpr int NS = L::kStages;
+  constexpr int MQ = L::kMq;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + NS;
+  uint64_t* s_full = q_empty + NS;  // each of these is [2], indexed by step buffer
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* p_full = dp_full + 2;
+  uint64_t* ds_full = p_full + 2;
+  uint64_t* sp_empty = ds_full + 2;
+  uint64_t* dq_full = sp_empty + 2;
+  uint64_t* dq_empty = dq_full + 2;
+  uint64_t* ds_empty = dq_empty + 2;
+  uint64_t* done = ds_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // head-major order (a head's Q and dO stay in L2 while its key tiles run);
+  // low key tiles, which see the most causal query rows, first
+  const int bh = blockIdx.x / p.n_kv_tiles;
+  const int kv_tile = blockIdx.x - bh * p.n_kv_tiles;
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
+  const int k0 = kv_tile * 128;
+  const int n_qt = (p.Sq + MQ - 1) / MQ;
+  const int qt_first = CAUSAL ? min(k0 / MQ, n_qt) : 0;
+  const int n_steps = n_qt - qt_first;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&dp_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&ds_full[x], 128);
+      mbar_init(&sp_empty[x], 128);
+      mbar_init(&dq_full[x], 1);
+      mbar_init(&dq_empty[x], 128);
+      mbar_init(&ds_empty[x], 1);
+    }
+    mbar_init(done, 1);
+    *abort_word = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 12) {
+    tmem_alloc(tmem_holder, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl wc{abort_word, p.err, p.wait_limit_ns};
+
+  if (warp == 13) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_steps > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * L::kKvBytes);
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, k0, h, b);
+        tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, k0, h, b);
+      }
+      for (int t = 0; t < n_steps; ++t) {
+        const int st = t % NS;
+        const int i0 = (qt_first + t) * MQ;
+        if (t >= NS) mbar_wait(&q_empty[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
+        mbar_arrive_expect_tx(&q_full[st], 2 * L::kQBytes + 2 * MQ * 4);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          tma_load_4d(smem + L::kQ + st * L::kQBytes + s * L::kQSlab, &tm_q, &q_full[st], s * 64,
+                      i0, h, b);
+          tma_load_4d(smem + L::kDO + st * L::kQBytes + s * L::kQSlab, &tm_do, &q_full[st],
+                      s * 64, i0, h, b);
+        }
+        const size_t vec = static_cast<size_t>(bh) * p.Sq_pad + i0;
+        bulk_load(smem + L::kLse + st * MQ * 4, p.lse2 + vec, MQ * 4, &q_full[st]);
+        bulk_load(smem + L::kDelta + st * MQ * 4, p.delta + vec, MQ * 4, &q_full[st]);
+      }
+      if (*abort_word) {
+        for (int t = max(0, n_steps - NS); t < n_steps; ++t)
+          mbar_wait_drain(&q_full[t % NS], (t / NS) & 1, 2000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 12) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_steps > 0) {
+      constexpr uint32_t kIdSP = idesc_bf16_f32(128, MQ, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdKV = idesc_bf16_f32(128, 128, false, true);  // dV, dK
+      constexpr uint32_t kIdQ = idesc_bf16_f32(128, MQ, true, true);     // dQ^T
+      const uint32_t ka = sb + L::kK, va = sb + L::kV;
+      // dV, dK and dQ of step u (buffer u & 1, stage u % NS)
+      auto finish_step = [&](int u) {
+        const int x = u & 1;
+        const int st = u % NS;
+        const uint32_t qa = sb + L::kQ + st * L::kQBytes;
+        const uint32_t oa = sb + L::kDO + st * L::kQBytes;
+        const uint32_t da = sb + L::kDs + x * L::kDsBytes;
+        mbar_wait(&p_full[x], (u >> 1) & 1, wc, kSiteBwdPFull);
+        tc_fence_after();
+        // dV += P~^T dO: A = P~^T bf16 in TMEM (32 columns), B = dO MN-major
+#pragma unroll
+        for (int kk = 0; kk < MQ / 16; ++kk)
+          mma_bf16_ts(tmem + L::kTmemDV, tmem + L::tmem_s(x) + kk * 8,
+                      sdesc_sw128(oa + kk * 2048, L::kQSlab, 1024), kIdKV,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        mbar_wait(&ds_full[x], (u >> 1) & 1, wc, kSiteBwdDsFull);
+        tc_fence_after();
+        // dK += dS^T Q: A = dS^T smem K-major, B = Q MN-major
+#pragma unroll
+        for (int kk = 0; kk < MQ / 16; ++kk)
+          mma_bf16_ss(tmem + L::kTmemDK, sdesc_sw128(da + kk * 32, 16, 1024),
+                      sdesc_sw128(qa + kk * 2048, L::kQSlab, 1024), kIdKV,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        // dQ^T [D x MQ] = K^T dS^T: A = K tile MN-major, B = dS^T MN-major; it
+        // overwrites this step's S^T columns (dV has read P~^T from them)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tmem + L::tmem_s(x), sdesc_sw128(ka + kk * 2048, L::kKvSlab, 1024),
+                      sdesc_sw128(da + kk * 2048, L::kDsBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
+        mma_commit(&dq_full[x]);
+        mma_commit(&q_empty[st]);
+        mma_commit(&ds_empty[x]);
+      };
+      mbar_wait(kv_full, 0, wc, kSiteBwdKvFull);
+      for (int t = 0; t < n_steps; ++t) {
+        const int x = t & 1;
+        const int st = t % NS;
+        const uint32_t qa = sb + L::kQ + st * L::kQBytes;
+        const uint32_t oa = sb + L::kDO + st * L::kQBytes;
+        mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
+        if (t >= 2) {
+          // step buffer x: scores read by its compute warpgroup, dQ^T(t-2) read out
+          mbar_wait(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
+          mbar_wait(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
+          mma_bf16_ss(tmem + L::tmem_s(x), sdesc_sw128(ka + koff, 16, 1024),
+                      sdesc_sw128(qa + qoff, 16, 1024), kIdSP, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[x]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
+          mma_bf16_ss(tmem + L::tmem_dp(x), sdesc_sw128(va + koff, 16, 1024),
+                      sdesc_sw128(oa + qoff, 16, 1024), kIdSP, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&dp_full[x]);
+        if (t >= 1) finish_step(t - 1);
+      }
+      finish_step(n_steps - 1);
+      mma_commit(done);
+      mbar_wait_drain(done, 0, 2000000000ull);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warpgroups A, B
+    const int x = warp >> 2;  // step parity handled by this warpgroup
+    const int r = threadIdx.x & 127;
+    const int kj = k0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + L::tmem_s(x) + lane_base;
+    const uint32_t tDP = tmem + L::tmem_dp(x) + lane_base;
+    const uint32_t da = sb + L::kDs + x * L::kDsBytes;
+    for (int t = x, k = 0; t < n_steps; t += 2, ++k) {
+      const int st = t % NS;
+      const int i0 = (qt_first + t) * MQ;
+      const uint32_t lse_s = sb + L::kLse + st * MQ * 4;
+      const uint32_t del_s = sb + L::kDelta + st * MQ * 4;
+      mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
+      mbar_wait(&s_full[x], k & 1, wc, kSiteBwdSFull);
+      tc_fence_after();
+      float pv[MQ];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tS, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld_wait(r0);
+        touch32(r1);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          pv[c] = __uint_as_float(r0[c]);
+          pv[32 + c] = __uint_as_float(r1[c]);
+        }
+      }
+      const bool need_mask = (k0 + 128 > p.Sk) || (CAUSAL && i0 < k0 + 127);
+      const int first_vis = kj >= p.Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
+#pragma unroll
+      for (int c = 0; c < MQ; ++c) {
+        float e = ex2_approx(fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4)));
+        if (need_mask && c < first_vis) e = 0.f;
+        pv[c] = e;
+      }
+      uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
+      if (DROPOUT) {
+        const uint64_t n_base =
+            (static_cast<uint64_t>(bh) * p.Sq + i0) * static_cast<uint64_t>(p.Sk) + kj;
+#pragma unroll
+        for (int c = 0; c < MQ; ++c) {
+          const bool kp =
+              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, p.pk);
+          if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
+        }
+      }
+      {
+        // P~^T (bf16) into this step's S^T columns [0, 32) of TMEM
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 2 * c;
+          float a = pv[e], bb = pv[e + 1];
+          if (DROPOUT) {
+            a = ((kb[e >> 5] >> (e & 31)) & 1u) ? a * p.drop_rescale : 0.f;
+            bb = ((kb[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? bb * p.drop_rescale : 0.f;
+          }
+          pk[c] = pack_bf16x2(a, bb);
+        }
+        tmem_st32(tS, pk);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&p_full[x]);
+
+      mbar_wait(&dp_full[x], k & 1, wc, kSiteBwdDpFull);
+      tc_fence_after();
+      if (k >= 1) mbar_wait(&ds_empty[x], (k - 1) & 1, wc, kSiteBwdPdsEmpty);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t d[32];
+        tmem_ld32(tDP + cc * 32, d);
+        tmem_ld_wait(d);
+        float ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = cc * 32 + i;
+          float g = __uint_as_float(d[i]);
+          if (DROPOUT) g = ((kb[cc] >> i) & 1u) ? g * p.drop_rescale : 0.f;
+          ds[i] = pv[e] * (g - ld_shared_f32(del_s + e * 4));
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int c = cc * 4 + q4;  // 16-byte chunk along the 128-byte row
+          st_shared_v4(da + sw128_offset(r, c), pack_bf16x2(ds[8 * q4 + 0], ds[8 * q4 + 1]),
+                       pack_bf16x2(ds[8 * q4 + 2], ds[8 * q4 + 3]),
+                       pack_bf16x2(ds[8 * q4 + 4], ds[8 * q4 + 5]),
+                       pack_bf16x2(ds[8 * q4 + 6], ds[8 * q4 + 7]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sp_empty[x]);
+      fence_async_smem();
+      mbar_arrive(&ds_full[x]);
+    }
+  } else {
+    // ------------------------------------------------------------ dQ warpgroup (warps 8-11)
+    const int lt = threadIdx.x - 256;  // TMEM lane = d
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t qa = sb + L::kDq;
+    for (int t = 0; t < n_steps; ++t) {
+      const int x = t & 1;
+      const int i0 = (qt_first + t) * MQ;
+      mbar_wait(&dq_full[x], (t >> 1) & 1, wc, kSiteBwdDqFull);
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tmem + L::tmem_s(x) + lane_base, r0);
+      tmem_ld32(tmem + L::tmem_s(x) + lane_base + 32, r1);
+      tmem_ld_wait(r0);
+      touch32(r1);
+      tc_fence_before();
+      mbar_arrive(&dq_empty[x]);
+      if (lt == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
+      named_barrier_sync(2, 128);
+      // lane = d, columns = query rows; the staging tile is row-major [MQ][D] fp32
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        st_shared_f32(qa + (c * 128 + lt) * 4, __uint_as_float(r0[c]));
+        st_shared_f32(qa + ((32 + c) * 128 + lt) * 4, __uint_as_float(r1[c]));
+      }
+      fence_async_smem();
+      named_barrier_sync(2, 128);
+      if (lt == 0) {
+        bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + i0) * 128,
+                            smem + L::kDq, L::kDqBytes);
+        bulk_commit();
+      }
+    }
+    if (lt == 0) bulk_wait_all();
+  }
+
+  // ------------------------------------------------------------ epilogue: dV (A), dK (B)
+  if (warp < 8) {
+    const bool is_dv = warp < 4;
+    const int r = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t acc = tmem + (is_dv ? L::kTmemDV : L::kTmemDK) + lane_base;
+    const uint32_t stage = sb + (is_dv ? L::kK : L::kV);  // K/V tiles are dead after `done`
+    const float mul = is_dv ? 1.f : p.scale;
+    if (n_steps > 0) {
+      mbar_wait(done, 0, wc, kSiteBwdDone);
+      tc_fence_after();
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      if (n_steps > 0) {
+        uint32_t o[32];
+        tmem_ld32(acc + c * 32, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(o[i]) * mul;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int col0 = c * 32 + q4 * 8;
+        st_shared_v4(stage + (col0 >> 6) * L::kKvSlab + sw128_offset(r, (col0 & 63) >> 3),
+                     pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]),
+                     pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
+                     pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
+                     pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
+      }
+    }
+    fence_async_smem();
+    named_barrier_sync(is_dv ? 3 : 4, 128);
+    if (r == 0) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
+                     s * 64, k0, h, b);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 12) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <bool C, bool DR>
+cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
+  auto kern = bwd_main_kernel_d128<C, DR>;
+  const int smem = B128::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
+  kern<<<grid, B128::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_d128_smem_bytes() { return B128::kAlloc; }
+
+cudaError_t launch_bwd_main_d128(bool causal, bool dropout, const CUtensorMap* maps,
+                                 const BwdParams& p, cudaStream_t stream) {
+  if (causal && dropout) return launch_t<true, true>(maps, p, stream);
+  if (causal) return launch_t<true, false>(maps, p, stream);
+  if (dropout) return launch_t<false, true>(maps, p, stream);
+  return launch_t<false, false>(maps, p, stream);
+}
+
+}  // namespace sdpa
