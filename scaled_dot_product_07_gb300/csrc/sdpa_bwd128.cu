@@ -180,50 +180,55 @@ __global__ void __launch_bounds__(448, 1)
     __syncwarp();
   } else if (warp == 12) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // The whole warp runs this loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues the tcgen05 instructions.
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();
       constexpr uint32_t kIdSP = idesc_bf16_f32(128, MQ, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(128, 128, false, true);  // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, MQ, true, true);     // dQ^T
-      const uint32_t ka = sb + L::kK, va = sb + L::kV;
+      // descriptor bases; per-MMA steps add compile-time offsets
+      const uint64_t kd_k = sdesc_sw128(sb + L::kK, 16, 1024);          // K, K-major
+      const uint64_t kd_v = sdesc_sw128(sb + L::kV, 16, 1024);          // V, K-major
+      const uint64_t kd_kmn = sdesc_sw128(sb + L::kK, L::kKvSlab, 1024);  // K as MN-major A
       // dV, dK and dQ of step u (buffer u & 1, stage u % NS)
       auto finish_step = [&](int u) {
         const int x = u & 1;
         const int st = u % NS;
-        const uint32_t qa = sb + L::kQ + st * L::kQBytes;
-        const uint32_t oa = sb + L::kDO + st * L::kQBytes;
-        const uint32_t da = sb + L::kDs + x * L::kDsBytes;
+        const uint64_t d_qmn = sdesc_sw128(sb + L::kQ + st * L::kQBytes, L::kQSlab, 1024);
+        const uint64_t d_omn = sdesc_sw128(sb + L::kDO + st * L::kQBytes, L::kQSlab, 1024);
+        const uint64_t d_ds = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, 16, 1024);
+        const uint64_t d_dsmn = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, L::kDsBytes, 1024);
         mbar_wait(&p_full[x], (u >> 1) & 1, wc, kSiteBwdPFull);
         tc_fence_after();
         // dV += P~^T dO: A = P~^T bf16 in TMEM (32 columns), B = dO MN-major
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk)
-          mma_bf16_ts(tmem + L::kTmemDV, tmem + L::tmem_s(x) + kk * 8,
-                      sdesc_sw128(oa + kk * 2048, L::kQSlab, 1024), kIdKV,
-                      (u > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts_if(leader, tmem + L::kTmemDV, tmem + L::tmem_s(x) + kk * 8,
+                         sdesc_add(d_omn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
         mbar_wait(&ds_full[x], (u >> 1) & 1, wc, kSiteBwdDsFull);
         tc_fence_after();
         // dK += dS^T Q: A = dS^T smem K-major, B = Q MN-major
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk)
-          mma_bf16_ss(tmem + L::kTmemDK, sdesc_sw128(da + kk * 32, 16, 1024),
-                      sdesc_sw128(qa + kk * 2048, L::kQSlab, 1024), kIdKV,
-                      (u > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss_if(leader, tmem + L::kTmemDK, sdesc_add(d_ds, kk * 32),
+                         sdesc_add(d_qmn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
         // dQ^T [D x MQ] = K^T dS^T: A = K tile MN-major, B = dS^T MN-major; it
         // overwrites this step's S^T columns (dV has read P~^T from them)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tmem + L::tmem_s(x), sdesc_sw128(ka + kk * 2048, L::kKvSlab, 1024),
-                      sdesc_sw128(da + kk * 2048, L::kDsBytes, 1024), kIdQ, kk > 0 ? 1u : 0u);
-        mma_commit(&dq_full[x]);
-        mma_commit(&q_empty[st]);
-        mma_commit(&ds_empty[x]);
+          mma_bf16_ss_if(leader, tmem + L::tmem_s(x), sdesc_add(kd_kmn, kk * 2048),
+                         sdesc_add(d_dsmn, kk * 2048), kIdQ, kk > 0 ? 1u : 0u);
+        mma_commit_if(leader, &dq_full[x]);
+        mma_commit_if(leader, &q_empty[st]);
+        mma_commit_if(leader, &ds_empty[x]);
       };
       mbar_wait(kv_full, 0, wc, kSiteBwdKvFull);
       for (int t = 0; t < n_steps; ++t) {
         const int x = t & 1;
         const int st = t % NS;
-        const uint32_t qa = sb + L::kQ + st * L::kQBytes;
-        const uint32_t oa = sb + L::kDO + st * L::kQBytes;
+        const uint64_t d_q = sdesc_sw128(sb + L::kQ + st * L::kQBytes, 16, 1024);
+        const uint64_t d_o = sdesc_sw128(sb + L::kDO + st * L::kQBytes, 16, 1024);
         mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
         if (t >= 2) {
           // step buffer x: scores read by its compute warpgroup, dQ^T(t-2) read out
@@ -231,26 +236,27 @@ __global__ void __launch_bounds__(448, 1)
           mbar_wait(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
         }
         tc_fence_after();
+        // S^T = K Q^T and dP~^T = V dO^T  (M = 128 keys, N = MQ, K = D)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::tmem_s(x), sdesc_sw128(ka + koff, 16, 1024),
-                      sdesc_sw128(qa + qoff, 16, 1024), kIdSP, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_if(leader, tmem + L::tmem_s(x), sdesc_add(kd_k, koff), sdesc_add(d_q, qoff),
+                         kIdSP, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[x]);
+        mma_commit_if(leader, &s_full[x]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::tmem_dp(x), sdesc_sw128(va + koff, 16, 1024),
-                      sdesc_sw128(oa + qoff, 16, 1024), kIdSP, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_if(leader, tmem + L::tmem_dp(x), sdesc_add(kd_v, koff), sdesc_add(d_o, qoff),
+                         kIdSP, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&dp_full[x]);
+        mma_commit_if(leader, &dp_full[x]);
         if (t >= 1) finish_step(t - 1);
       }
       finish_step(n_steps - 1);
-      mma_commit(done);
+      mma_commit_if(leader, done);
       mbar_wait_drain(done, 0, 2000000000ull);
     }
     __syncwarp();
