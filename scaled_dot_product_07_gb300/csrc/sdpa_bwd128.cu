@@ -7,7 +7,8 @@
 // One CTA per 128-key tile of one (batch, head); it walks the 64-row query
 // steps that can see its keys. 448 threads:
 //   warp 13     TMA: K, V once; Q_t, dO_t, lse2_t, Delta_t through a 3-stage ring
-//   warp 12     TMEM allocator and MMA issuer (one thread)
+//   warp 12     TMEM allocator and MMA issuer (the warp runs converged; one
+//               elected lane issues the tcgen05 instructions)
 //   warps 0-3   compute warpgroup A (even steps), warps 4-7 B (odd steps):
 //               thread = key row. P^T = exp2(S^T*scale*log2e - lse2) (masked,
 //               dropout applied) is stored as bf16 into TMEM (A operand of

@@ -8,7 +8,8 @@
 // (batch, head), 320 threads:
 //   warp 9      TMA producer: Q0, Q1 once, then K_j and V_j (separate
 //               barriers) through a ring of 128-byte-swizzled stages.
-//   warp 8      TMEM allocator and MMA issuer (one thread). TMEM holds
+//   warp 8      TMEM allocator and MMA issuer (the warp runs converged, one
+//               elected lane issues the tcgen05 instructions). TMEM holds
 //               S0, S1 (128 fp32 columns each) and O0, O1 (D columns each).
 //               Per key tile j it issues, in this order,
 //                 O0 += P0_j V_j,  S0_{j+1} = Q0 K_{j+1}^T,
@@ -176,56 +177,56 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      auto issue_s = [&](int i, int j) {
-        const int st = j % S;
-        const uint32_t qa = sb + L::kQ + i * L::kTileBytes;
-        const uint32_t ka = sb + L::kK + st * L::kTileBytes;
+    // The whole warp runs this loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues the tcgen05 instructions.
+    const uint32_t leader = elect_one();
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+    auto issue_s = [&](int i, int j) {
+      const int st = j % S;
+      const uint64_t qd = sdesc_sw128(sb + L::kQ + i * L::kTileBytes, 16, 1024);
+      const uint64_t kd = sdesc_sw128(sb + L::kK + st * L::kTileBytes, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + L::tmem_s(i), sdesc_sw128(qa + koff, 16, 1024),
-                      sdesc_sw128(ka + koff, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[i]);
-      };
-      auto issue_pv = [&](int i, int j) {
-        const int st = j % S;
-        const uint32_t va = sb + L::kV + st * L::kTileBytes;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
+        mma_bf16_ss_if(leader, tmem + L::tmem_s(i), sdesc_add(qd, koff), sdesc_add(kd, koff), kIdS,
+                       kk > 0 ? 1u : 0u);
+      }
+      mma_commit_if(leader, &s_full[i]);
+    };
+    auto issue_pv = [&](int i, int j) {
+      const int st = j % S;
+      const uint64_t vd = sdesc_sw128(sb + L::kV + st * L::kTileBytes, L::kSlabBytes, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + L::tmem_o(i), tmem + L::tmem_s(i) + kk * 8,
-                      sdesc_sw128(va + kk * 2048, L::kSlabBytes, 1024), kIdO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      mbar_wait(q_full, 0, wc, kSiteFwdQFull);
-      if (n_kv > 0) {
-        mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts_if(leader, tmem + L::tmem_o(i), tmem + L::tmem_s(i) + kk * 8,
+                       sdesc_add(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    mbar_wait(q_full, 0, wc, kSiteFwdQFull);
+    if (n_kv > 0) {
+      mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+      tc_fence_after();
+      for (int i = 0; i < 2; ++i)
+        if (n_t[i] > 0) issue_s(i, 0);
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j % S;
+      mbar_wait(&v_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
+      for (int i = 0; i < 2; ++i) {
+        if (j >= n_t[i]) continue;
+        mbar_wait(&p_full[i], j & 1, wc, kSiteFwdPFull);
         tc_fence_after();
-        for (int i = 0; i < 2; ++i)
-          if (n_t[i] > 0) issue_s(i, 0);
-      }
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        mbar_wait(&v_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
-        for (int i = 0; i < 2; ++i) {
-          if (j >= n_t[i]) continue;
-          mbar_wait(&p_full[i], j & 1, wc, kSiteFwdPFull);
+        issue_pv(i, j);
+        if (j + 1 < n_t[i]) {
+          const int st1 = (j + 1) % S;
+          mbar_wait(&k_full[st1], ((j + 1) / S) & 1, wc, kSiteFwdKvFull);
           tc_fence_after();
-          issue_pv(i, j);
-          if (j + 1 < n_t[i]) {
-            const int st1 = (j + 1) % S;
-            mbar_wait(&k_full[st1], ((j + 1) / S) & 1, wc, kSiteFwdKvFull);
-            tc_fence_after();
-            issue_s(i, j + 1);
-          } else {
-            mma_commit(&o_full[i]);
-          }
+          issue_s(i, j + 1);
+        } else {
+          mma_commit_if(leader, &o_full[i]);
         }
-        mma_commit(&kv_empty[st]);
       }
+      mma_commit_if(leader, &kv_empty[st]);
     }
     __syncwarp();
   } else {
