@@ -306,7 +306,10 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // The whole warp runs this loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues the tcgen05 instructions.
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();
       constexpr uint32_t kIdSP = idesc_bf16_f32(128, MQ, false, false);   // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(128, D, false, true);     // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, 64, true, true);      // dQ^T / dQ
@@ -326,25 +329,25 @@ __global__ void __launch_bounds__(320, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
-          mma_bf16_ss(tS, sdesc_sw128(ka + koff, 16, 1024), sdesc_sw128(qa + qoff, 16, 1024),
+          mma_bf16_ss_if(leader, tS, sdesc_sw128(ka + koff, 16, 1024), sdesc_sw128(qa + qoff, 16, 1024),
                       kIdSP, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
+        mma_commit_if(leader, s_full);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
-          mma_bf16_ss(tDP, sdesc_sw128(va + koff, 16, 1024), sdesc_sw128(oa + qoff, 16, 1024),
+          mma_bf16_ss_if(leader, tDP, sdesc_sw128(va + koff, 16, 1024), sdesc_sw128(oa + qoff, 16, 1024),
                       kIdSP, kk > 0 ? 1u : 0u);
         }
-        mma_commit(dp_full);
+        mma_commit_if(leader, dp_full);
         // dV += P~^T dO  (M = 128 keys, N = D, K = MQ; dO read MN-major)
         mbar_wait(p_full, t & 1, wc, kSiteBwdPFull);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * L::kPtSlab + (kk & 3) * 32;
-          mma_bf16_ss(tDV, sdesc_sw128(pa + poff, 16, 1024),
+          mma_bf16_ss_if(leader, tDV, sdesc_sw128(pa + poff, 16, 1024),
                       sdesc_sw128(oa + kk * 2048, L::kQSlab, 1024), kIdKV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         }
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk) {
           const uint32_t poff = (kk >> 2) * L::kPtSlab + (kk & 3) * 32;
-          mma_bf16_ss(tDK, sdesc_sw128(da + poff, 16, 1024),
+          mma_bf16_ss_if(leader, tDK, sdesc_sw128(da + poff, 16, 1024),
                       sdesc_sw128(qa + kk * 2048, L::kQSlab, 1024), kIdKV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         }
@@ -368,15 +371,15 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t kdesc = sdesc_sw128(ka + kk * 2048, L::kKvSlab, 1024);
           const uint64_t sdesc = sdesc_sw128(da + kk * 2048, L::kPtSlab, 1024);
           if constexpr (D == 128)
-            mma_bf16_ss(tDQ, kdesc, sdesc, kIdQ, kk > 0 ? 1u : 0u);
+            mma_bf16_ss_if(leader, tDQ, kdesc, sdesc, kIdQ, kk > 0 ? 1u : 0u);
           else
-            mma_bf16_ss(tDQ, sdesc, kdesc, kIdQ, kk > 0 ? 1u : 0u);
+            mma_bf16_ss_if(leader, tDQ, sdesc, kdesc, kIdQ, kk > 0 ? 1u : 0u);
         }
-        mma_commit(dq_full);
-        mma_commit(&q_empty[st]);
-        mma_commit(pds_empty);
+        mma_commit_if(leader, dq_full);
+        mma_commit_if(leader, &q_empty[st]);
+        mma_commit_if(leader, pds_empty);
       }
-      mma_commit(done);
+      mma_commit_if(leader, done);
       mbar_wait_drain(done, 0, 2000000000ull);
     }
     __syncwarp();

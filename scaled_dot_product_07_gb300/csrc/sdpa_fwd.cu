@@ -44,8 +44,8 @@ struct FwdLayout {
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kBar = kV + kStages * kTileBytes;
-  // q_full, k_full[S], v_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2]
-  static constexpr int kNumBars = 1 + 3 * kStages + 6;
+  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full[2]
+  static constexpr int kNumBars = 1 + 4 * kStages + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;             // room to align to 1024
@@ -90,8 +90,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
   uint64_t* v_full = k_full + S;
-  uint64_t* kv_empty = v_full + S;
-  uint64_t* s_full = kv_empty + S;   // [2]
+  uint64_t* k_empty = v_full + S;
+  uint64_t* v_empty = k_empty + S;
+  uint64_t* s_full = v_empty + S;    // [2]
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_full = p_full + 2;     // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -118,7 +119,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -154,12 +156,15 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
-        if (j >= S) mbar_wait(&kv_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
+        // a K stage is free once the last S MMA reading it is done, a V stage
+        // once the last P V MMA reading it is done
+        if (j >= S) mbar_wait(&k_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
         mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
                       s * 64, j * 128, h, b);
+        if (j >= S) mbar_wait(&v_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
         mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
@@ -208,6 +213,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       for (int i = 0; i < 2; ++i)
         if (n_t[i] > 0) issue_s(i, 0);
+      mma_commit_if(leader, &k_empty[0]);  // K_0 has no other reader
     }
     for (int j = 0; j < n_kv; ++j) {
       const int st = j % S;
@@ -226,7 +232,8 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit_if(leader, &o_full[i]);
         }
       }
-      mma_commit_if(leader, &kv_empty[st]);
+      mma_commit_if(leader, &v_empty[st]);                             // V_j read by both P V
+      if (j + 1 < n_kv) mma_commit_if(leader, &k_empty[(j + 1) % S]);  // K_{j+1} by both S
     }
     __syncwarp();
   } else {
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       float mx = fmaxf(x[0], x[1]);
 #pragma unroll
-      for (int c = 2; c < 128; c += 2) mx = fmaxf(mx, fmaxf(x[c], x[c + 1]));
+      for (int c = 2; c < 128; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
