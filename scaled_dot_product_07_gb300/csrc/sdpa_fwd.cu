@@ -277,9 +277,15 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) x[c] = -INFINITY;
       }
-      float mx = fmaxf(x[0], x[1]);
+      // row max as 8 independent chains (short dependency depth), then combined
+      float mp[8];
 #pragma unroll
-      for (int c = 2; c < 128; c += 2) mx = fmax3(mx, x[c], x[c + 1]);
+      for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
+#pragma unroll
+      for (int c = 16; c < 128; c += 16)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
+      const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
       const float m_new = fmaxf(m, mx);
       if (j == 0) {
         m = m_new;
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
 
       uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (DROPOUT) keep_bits_128(n_row + k0, p.drop_threshold, p.pk, keep);
-      float rs0 = 0.f, rs1 = 0.f;
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk2[32];
@@ -311,8 +317,7 @@ __global__ void __launch_bounds__(320, 1)
           const int e = hf * 64 + c;
           float e0 = ex2_approx(fmaf(x[e], sl2, neg));
           float e1 = ex2_approx(fmaf(x[e + 1], sl2, neg));
-          rs0 += e0;
-          rs1 += e1;
+          rs[(c >> 1) & 7] += e0 + e1;
           if (DROPOUT) {
             e0 = ((keep[e >> 5] >> (e & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
             e1 = ((keep[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(320, 1)
         // P columns [32 hf, 32 hf + 32) overwrite scores already held in registers
         tmem_st32(tS + hf * 32, pk2);
       }
-      l += rs0 + rs1;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[i]);
