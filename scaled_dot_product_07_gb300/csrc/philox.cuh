@@ -51,24 +51,27 @@ __device__ __forceinline__ uint4 philox_group(uint64_t g, const PhiloxKey& pk) {
                        pk.off_hi, pk.k0, pk.k1);
 }
 
-// Keep bits of the 128 consecutive absolute indices n0 .. n0+127:
+// Keep bits of the 32*W consecutive absolute indices n0 .. n0+32W-1:
 // bit e of bits[e/32] is 1 iff element n0+e is kept.
-__device__ __forceinline__ void keep_bits_128(uint64_t n0, uint32_t threshold, const PhiloxKey& pk,
-                                              uint32_t (&bits)[4]) {
+template <int W>
+__device__ __forceinline__ void keep_bits(uint64_t n0, uint32_t threshold, const PhiloxKey& pk,
+                                          uint32_t (&bits)[W]) {
   const uint64_t g0 = n0 >> 2;
   const uint32_t a = static_cast<uint32_t>(n0 & 3u);
-  // 33 groups cover n0 .. n0+127 for any alignment a; stream bit 4t+w holds
+  // 8W+1 groups cover the range for any alignment a; stream bit 4t+w holds
   // the decision of n = 4(g0+t)+w, i.e. of element e = 4t+w-a.
-  uint32_t s[5] = {0u, 0u, 0u, 0u, 0u};
+  uint32_t s[W + 1];
 #pragma unroll
-  for (int t = 0; t < 33; ++t) {
+  for (int i = 0; i <= W; ++i) s[i] = 0u;
+#pragma unroll
+  for (int t = 0; t < 8 * W + 1; ++t) {
     const uint4 u = philox_group(g0 + t, pk);
     const uint32_t nib = (u.x >= threshold ? 1u : 0u) | (u.y >= threshold ? 2u : 0u) |
                          (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
     s[(4 * t) / 32] |= nib << ((4 * t) % 32);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) bits[i] = __funnelshift_r(s[i], s[i + 1], a);
+  for (int i = 0; i < W; ++i) bits[i] = __funnelshift_r(s[i], s[i + 1], a);
 }
 
 // Keep bit of one absolute index.

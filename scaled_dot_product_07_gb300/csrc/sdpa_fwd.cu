@@ -14,18 +14,23 @@
 //               Per key tile j it issues, in this order,
 //                 O0 += P0_j V_j,  S0_{j+1} = Q0 K_{j+1}^T,
 //                 O1 += P1_j V_j,  S1_{j+1} = Q1 K_{j+1}^T,
-//               so that while one softmax warpgroup works on its scores the
+//               so that while the softmax works on one tile's scores the
 //               tensor core runs the other tile's products (ping-pong).
 //               P_i is bf16 written by the softmax into the first 64 columns
 //               of S_i and is read straight from TMEM as the A operand.
-//   warps 0-3   softmax of Q0, warps 4-7 softmax of Q1: thread r owns query
-//               row r of its tile. Per key tile it loads the score row, masks
-//               the causal diagonal / key tail, keeps the running row max m
-//               and sum l, rescales its O row in TMEM only when the max grew
-//               by more than 2^8 (exact: the shift only changes the common
-//               reference), and stores P (bf16, dropout applied) into TMEM.
-//               At the end it writes out = O / l (TMA store through shared
-//               memory) and lse = m * scale + ln l.
+//   warps 0-7   softmax, both warpgroups on the same tile (Q0's scores,
+//               then Q1's): warps w and w+4 share TMEM lanes, so thread
+//               (half, r) owns keys [64 half, 64 half + 64) of query row r.
+//               Per key tile it loads its half row, masks the causal
+//               diagonal / key tail, agrees on the row max with its partner
+//               half (shared memory + 64-thread named barrier), rescales its
+//               half of the O row in TMEM only when the max grew by more
+//               than 2^8 (exact: the shift only changes the common
+//               reference), and stores its half of P (bf16, dropout
+//               applied) into TMEM. Halving the work per thread halves the
+//               softmax latency each tile adds to the ping-pong. At the end
+//               the halves' row sums are combined and out = O / l (TMA store
+//               through shared memory) and lse = m * scale + ln l written.
 // The completion of S_i(j+1) implies that O_i += P_i(j) V_j has completed
 // (tcgen05 operations of one issuing thread complete in order), so the
 // softmax may touch O_i as soon as it sees its next scores.
@@ -43,7 +48,10 @@ struct FwdLayout {
   static constexpr int kQ = 0;                            // Q0, Q1
   static constexpr int kK = kQ + 2 * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBar = kV + kStages * kTileBytes;
+  // row-max / row-sum exchange between the two halves of a row:
+  // [tile 2][parity 2][half 2][row 128] fp32
+  static constexpr int kRed = kV + kStages * kTileBytes;
+  static constexpr int kBar = kRed + 2 * 2 * 2 * 128 * 4;
   // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full[2]
   static constexpr int kNumBars = 1 + 4 * kStages + 6;
   static constexpr int kMisc = kBar + kNumBars * 8;
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 256);
       mbar_init(&o_full[i], 1);
     }
     *abort_word = 0u;
@@ -237,116 +245,143 @@ __global__ void __launch_bounds__(320, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int i = warp >> 2;          // query tile of this warpgroup
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    // Both warpgroups work on the same tile: warp w and warp w+4 share TMEM
+    // lanes, so thread (half, r) handles key columns [64h, 64h+64) of query row
+    // r. The two halves of a row agree on its max through shared memory and
+    // a 64-thread named barrier per warp pair; their partial row sums are
+    // combined only at the end.
+    const int half = warp >> 2;         // half of the key columns
     const int row = threadIdx.x & 127;  // row in the tile == TMEM lane
-    const int qi = q0 + 128 * i + row;
-    const int n_mine = n_t[i];
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
-    const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-    const uint64_t n_row = (static_cast<uint64_t>(bh) * p.Sq + qi) * static_cast<uint64_t>(p.Sk);
+    const uint32_t pair_bar = 1 + (warp & 3);  // + 4 * tile
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of the raw scores of this row
-    float l = 0.f;
-
-    for (int j = 0; j < n_mine; ++j) {
-      mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
+    float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
+    float l[2] = {0.f, 0.f};              // this half's running sum, per tile
+    // the half's tile max, shared with the partner half; returns the row's tile max
+    auto exchange_max = [&](int i, int j, float mh) {
+      float* slot = red + ((i * 2 + (j & 1)) * 2) * 128;
+      slot[half * 128 + row] = mh;
+      // also orders the partner's TMEM score reads before this warp's P
+      // stores into the same columns
+      tc_fence_before();
+      named_barrier_sync(pair_bar + 4 * i, 64);
       tc_fence_after();
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS + 0, r0);
-      tmem_ld32(tS + 32, r1);
-      tmem_ld32(tS + 64, r2);
-      tmem_ld32(tS + 96, r3);
-      tmem_ld_wait(r0);
-      reg_touch(r1);
-      reg_touch(r2);
-      reg_touch(r3);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        x[c] = __uint_as_float(r0[c]);
-        x[32 + c] = __uint_as_float(r1[c]);
-        x[64 + c] = __uint_as_float(r2[c]);
-        x[96 + c] = __uint_as_float(r3[c]);
-      }
-      const int k0 = j * 128;
-      if ((k0 + 128 > p.Sk) || (CAUSAL && k0 + 127 > q0 + 128 * i)) {
-        const int lim = CAUSAL ? min(p.Sk - k0, qi - k0 + 1) : (p.Sk - k0);
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) x[c] = -INFINITY;
-      }
-      // row max as 8 independent chains (short dependency depth), then combined
-      float mp[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
-#pragma unroll
-      for (int c = 16; c < 128; c += 16)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
-      const float mx = fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
-      const float m_new = fmaxf(m, mx);
-      if (j == 0) {
-        m = m_new;
-      } else if (__any_sync(0xffffffffu, (m_new - m) * sl2 > 8.0f)) {
-        // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
-        const float alpha = ex2_approx((m - m_new) * sl2);
-        l *= alpha;
-        m = m_new;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
-      const float neg = -m * sl2;
+      return fmaxf(mh, slot[(1 - half) * 128 + row]);
+    };
 
-      uint32_t keep[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (DROPOUT) keep_bits_128(n_row + k0, p.drop_threshold, p.pk, keep);
-      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
+    for (int j = 0; j < n_kv; ++j) {
+      for (int i = 0; i < 2; ++i) {
+        if (j >= n_t[i]) continue;
+        const int qi = q0 + 128 * i + row;
+        const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
+        const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+        mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tS + 64 * half, r0);
+        tmem_ld32(tS + 64 * half + 32, r1);
+        tmem_ld_wait(r0);
+        reg_touch(r1);
+        float x[64];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0[c]);
+          x[32 + c] = __uint_as_float(r1[c]);
+        }
+        const int k0 = j * 128 + 64 * half;  // first key of this half
+        if ((k0 + 64 > p.Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
+          const int lim = CAUSAL ? min(p.Sk - k0, qi - k0 + 1) : (p.Sk - k0);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= lim) x[c] = -INFINITY;
+        }
+        // half-row max as 8 independent chains, then combined
+        float mp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
+#pragma unroll
+        for (int c = 16; c < 64; c += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
+        const float mh =
+            fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
+        const float m_new = fmaxf(m[i], exchange_max(i, j, mh));
+        if (j == 0) {
+          m[i] = m_new;
+        } else if (__any_sync(0xffffffffu, (m_new - m[i]) * sl2 > 8.0f)) {
+          // both halves of these rows take this branch (same rows, same maxima);
+          // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
+          const float alpha = ex2_approx((m[i] - m_new) * sl2);
+          l[i] *= alpha;
+          m[i] = m_new;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
+            uint32_t o[32];
+            tmem_ld32(tO + (D / 2) * half + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + (D / 2) * half + c * 32, o);
+          }
+        }
+        const float neg = -m[i] * sl2;
+
+        uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
+        if (DROPOUT) {
+          const uint64_t n_row =
+              (static_cast<uint64_t>(bh) * p.Sq + qi) * static_cast<uint64_t>(p.Sk);
+          keep_bits<2>(n_row + k0, p.drop_threshold, p.pk, keep);
+        }
+        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
         uint32_t pk2[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const int e = hf * 64 + c;
-          float e0 = ex2_approx(fmaf(x[e], sl2, neg));
-          float e1 = ex2_approx(fmaf(x[e + 1], sl2, neg));
+          float e0 = ex2_approx(fmaf(x[c], sl2, neg));
+          float e1 = ex2_approx(fmaf(x[c + 1], sl2, neg));
           rs[(c >> 1) & 7] += e0 + e1;
           if (DROPOUT) {
-            e0 = ((keep[e >> 5] >> (e & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
-            e1 = ((keep[(e + 1) >> 5] >> ((e + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
+            e0 = ((keep[c >> 5] >> (c & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
+            e1 = ((keep[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
           }
           pk2[c >> 1] = pack_bf16x2(e0, e1);
         }
-        // P columns [32 hf, 32 hf + 32) overwrite scores already held in registers
-        tmem_st32(tS + hf * 32, pk2);
+        // P (bf16 pairs) of keys [64h, 64h+64) -> S columns [32h, 32h+32); they
+        // overwrite scores this warp pair has already read
+        tmem_st32(tS + 32 * half, pk2);
+        l[i] += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[i]);
     }
 
     // ------------------------------------------------------------ epilogue
-    if (n_mine > 0) {
+    for (int i = 0; i < 2; ++i) {
+      if (n_t[i] == 0) continue;
+      const int qi = q0 + 128 * i + row;
+      const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+      // the row sum is the sum of both halves (slot parity n_t[i] is unused by
+      // the last tile's max exchange)
+      const float l_row = [&] {
+        float* slot = red + ((i * 2 + (n_t[i] & 1)) * 2) * 128;
+        slot[half * 128 + row] = l[i];
+        named_barrier_sync(pair_bar + 4 * i, 64);
+        return l[i] + slot[(1 - half) * 128 + row];
+      }();
       mbar_wait(&o_full[i], 0, wc, kSiteFwdODone);
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / l_row;
       const uint32_t oa = sb + L::kQ + i * L::kTileBytes;  // Q_i is dead after o_full[i]
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns
         uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
+        tmem_ld32(tO + (D / 2) * half + c * 32, o);
         tmem_ld_wait(o);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          const int col0 = c * 32 + q4 * 8;
+          const int col0 = (D / 2) * half + c * 32 + q4 * 8;
           const uint32_t addr =
               oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3);
           st_shared_v4(addr,
@@ -360,11 +395,11 @@ __global__ void __launch_bounds__(320, 1)
                                    __uint_as_float(o[q4 * 8 + 7]) * inv_l));
         }
       }
-      if (qi < p.Sq)
-        p.lse[static_cast<size_t>(bh) * p.Sq + qi] = m * (sl2 * kLn2) + __logf(l);
+      if (half == 0 && qi < p.Sq)
+        p.lse[static_cast<size_t>(bh) * p.Sq + qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
       fence_async_smem();
-      named_barrier_sync(1 + i, 128);
-      if (row == 0) {
+      named_barrier_sync(9 + i, 256);
+      if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_store_4d(&tm_o, smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, s * 64,
