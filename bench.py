@@ -16,6 +16,9 @@ e2e         the same metric through the public API with host buffers: each
             compute and a download stream.
 roofline    the backward (dominant) and forward kernels against the measured
             dense bf16 peak.
+extended    the options entry points on the same workload: the step recorded
+            once as a CUDA graph (rng state read from device memory) and
+            replayed, and the deterministic (fixed-order dQ) backward.
 cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
             the same workload (whole heads), on this host's cores.
 """
@@ -311,6 +314,61 @@ def bench_ours(args, w):
     pk, pk_src = peaks()
     peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
+    # ---- the extended entry points on the same workload: the step recorded
+    # once as a CUDA graph with the rng state read from device memory, and the
+    # deterministic (fixed-order dQ) backward
+    extras = None
+    if not args.no_extras:
+        extras = {}
+
+        def timed(fn, n):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n
+
+        rng = torch.tensor([w.seed, w.offset], dtype=torch.int64, device=dev)
+
+        def step_ex():
+            sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, rng_state=rng, out=out, lse=lse)
+            sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, rng_state=rng,
+                             dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step_ex()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step_ex()
+        g_ms = timed(graph.replay, max(5, min(args.steps, 20)))
+        extras["graph_step"] = {"ms": g_ms, "tflops": (f_fwd + f_bwd) / (g_ms * 1e-3) / 1e12,
+                                "note": "fwd+bwd captured once (sdpa_fwd_ex/sdpa_bwd_ex, rng "
+                                        "state in device memory), replayed"}
+        del graph
+        ws_det = torch.empty(sdpa.sdpa_bwd_workspace_size_ex(w.B, w.H, w.Sq, w.Sk, w.D, True),
+                             dtype=torch.uint8, device=dev)
+
+        def bwd_det():
+            sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset,
+                             deterministic=True, dq=dq, dk=dk, dv=dv, workspace=ws_det)
+
+        d_ms = timed(bwd_det, 5)
+        extras["bwd_deterministic"] = {
+            "ms": d_ms, "tflops": f_bwd / (d_ms * 1e-3) / 1e12, "workspace_bytes": ws_det.numel(),
+            "note": "one fp32 dQ partial per 128-key tile, summed in key-tile order"}
+        del ws_det
+        if sdpa.sdpa_check_device() != 0:
+            raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -404,6 +462,7 @@ def bench_ours(args, w):
                          "traffic": kernel_traffic("fwd_kernel"),
                          "peak_source": f"{pk_src} bf16_tflops (burst)"},
         "e2e": e2e,
+        "extended": extras,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
@@ -421,6 +480,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the CUDA-graph and deterministic-backward timings")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (small cases for profiling; not a bench line)")
     args = ap.parse_args()

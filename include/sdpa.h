@@ -159,6 +159,73 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
                                     uint8_t* mask, sdpa_stream_t stream);
 
 /*
+ * sdpa_options — extensions of the forward and backward calls (the *_ex entry
+ * points below). A zero-initialised struct, or a NULL pointer, gives exactly
+ * the behaviour of sdpa_fwd / sdpa_bwd / sdpa_dropout_mask_debug.
+ *
+ *   rng_state: NULL, or a device pointer (8-byte aligned) to two uint64
+ *     values {seed, offset} that the kernels read when they run, in place of
+ *     the seed and offset arguments. The rng state then travels from forward
+ *     to backward through device memory, so a captured CUDA graph can be
+ *     replayed with a new state written into that buffer between replays
+ *     (the graph-safe rng passing of "REDO of dropout support for mem eff
+ *     #102038", pytorch PR 103704, Summary). The buffer must hold the same
+ *     values when the backward runs as when the forward ran.
+ *   batch_offset, head_offset, total_heads: where this call's [B, H] block
+ *     sits in a larger problem that is split by batch and head across calls
+ *     or devices (the head split of test_sdpa_loop_split, "DID loop split for
+ *     SDPA", NVIDIA/Fuser PR 3711). The dropout counter uses the global
+ *     batch index batch_offset + b and head index head_offset + h out of
+ *     total_heads heads per batch, so each part draws exactly its slice of
+ *     the unsplit problem's mask. total_heads = 0 means H (no head split);
+ *     otherwise head_offset + H <= total_heads. Offsets must be >= 0.
+ *   deterministic: sdpa_bwd_ex only. Nonzero: every 128-key tile stores its
+ *     fp32 dQ partials into its own workspace slice and a final kernel adds
+ *     them in key-tile order, so dq is bitwise reproducible run to run (the
+ *     default reduce-adds partials into one accumulator in whatever order
+ *     the tiles finish). It needs the larger workspace that
+ *     sdpa_bwd_workspace_size_ex() reports and moves about twice the partials'
+ *     bytes through HBM.
+ */
+typedef struct {
+  const uint64_t* rng_state;
+  int64_t batch_offset;
+  int64_t head_offset;
+  int64_t total_heads;
+  int deterministic;
+} sdpa_options;
+
+/* sdpa_fwd with options (NULL options = sdpa_fwd). */
+sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                        double dropout_p, int is_causal, float scale, uint64_t seed,
+                        uint64_t offset, sdpa_tensor* out, float* lse,
+                        const sdpa_options* options, sdpa_stream_t stream);
+
+/*
+ * sdpa_bwd_workspace_size_ex — workspace bytes of sdpa_bwd_ex with these
+ * options: sdpa_bwd_workspace_size(), or in deterministic mode one fp32 dQ
+ * slice per 128-key tile, B*H*ceil128(Sq)*(D*ceil(Sk/128) + 2)*4 bytes.
+ */
+size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
+                                  const sdpa_options* options);
+
+/* sdpa_bwd with options (NULL options = sdpa_bwd); the workspace must have
+ * sdpa_bwd_workspace_size_ex() bytes for the same options. */
+sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                        const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                        double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                        float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                        void* workspace, size_t workspace_bytes, const sdpa_options* options,
+                        sdpa_stream_t stream);
+
+/* sdpa_dropout_mask_debug with options (rng_state and the batch/head
+ * position; `deterministic` is ignored). */
+sdpa_status sdpa_dropout_mask_debug_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                       double dropout_p, uint64_t seed, uint64_t offset,
+                                       const sdpa_options* options, uint8_t* mask,
+                                       sdpa_stream_t stream);
+
+/*
  * sdpa_check_device — synchronises `stream`, then reports whether any kernel
  * of this library on the current device gave up on a bounded wait since the
  * last check (SDPA_ERR_DEVICE_TIMEOUT; the word is cleared) or the stream

@@ -25,7 +25,8 @@ __all__ = [
     "SdpaError", "load_library", "library_path", "sdpa_fwd", "sdpa_bwd",
     "sdpa_bwd_workspace_size", "sdpa_dropout_mask_debug", "sdpa_check_device",
     "sdpa_selftest_wait_timeout", "sdpa_status_string", "SDPAFunction", "EXPORTED_SYMBOLS",
-    "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "sdpa_fwd_ex", "sdpa_bwd_ex",
+    "sdpa_bwd_workspace_size_ex", "sdpa_dropout_mask_debug_ex", "SdpaOptions",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +37,7 @@ _LIB = None
 EXPORTED_SYMBOLS = (
     "sdpa_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_dropout_mask_debug",
     "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string", "sdpa_bwd_noalloc",
+    "sdpa_fwd_ex", "sdpa_bwd_workspace_size_ex", "sdpa_bwd_ex", "sdpa_dropout_mask_debug_ex",
 )
 
 # SDPA_BWD_NOALLOC_SCRATCH_BYTES of include/sdpa.h
@@ -58,6 +60,13 @@ class SdpaError(RuntimeError):
 class SdpaTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("size", ctypes.c_int64 * 4),
                 ("stride", ctypes.c_int64 * 4)]
+
+
+class SdpaOptions(ctypes.Structure):
+    """sdpa_options of include/sdpa.h."""
+    _fields_ = [("rng_state", ctypes.c_void_p), ("batch_offset", ctypes.c_int64),
+                ("head_offset", ctypes.c_int64), ("total_heads", ctypes.c_int64),
+                ("deterministic", ctypes.c_int)]
 
 
 def library_path():
@@ -89,6 +98,15 @@ def load_library(path=None):
     lib.sdpa_bwd_noalloc.restype = ctypes.c_int
     lib.sdpa_dropout_mask_debug.argtypes = [i64, i64, i64, i64, dbl, u64, u64, vp, vp]
     lib.sdpa_dropout_mask_debug.restype = ctypes.c_int
+    lib.sdpa_fwd_ex.argtypes = [P, P, P, dbl, ctypes.c_int, flt, u64, u64, P, vp, vp, vp]
+    lib.sdpa_fwd_ex.restype = ctypes.c_int
+    lib.sdpa_bwd_workspace_size_ex.argtypes = [i64, i64, i64, i64, i64, vp]
+    lib.sdpa_bwd_workspace_size_ex.restype = ctypes.c_size_t
+    lib.sdpa_bwd_ex.argtypes = [P, P, P, P, P, vp, dbl, ctypes.c_int, u64, u64, flt, P, P, P, vp,
+                                ctypes.c_size_t, vp, vp]
+    lib.sdpa_bwd_ex.restype = ctypes.c_int
+    lib.sdpa_dropout_mask_debug_ex.argtypes = [i64, i64, i64, i64, dbl, u64, u64, vp, vp, vp]
+    lib.sdpa_dropout_mask_debug_ex.restype = ctypes.c_int
     lib.sdpa_check_device.argtypes = [vp]
     lib.sdpa_check_device.restype = ctypes.c_int
     lib.sdpa_selftest_wait_timeout.argtypes = [u64, vp]
@@ -235,6 +253,94 @@ def sdpa_dropout_mask_debug(B, H, Sq, Sk, dropout_p, seed, offset, device="cuda"
                                      ctypes.c_void_p(mask.data_ptr() if mask.numel() else None),
                                      _stream(mask.device))
     _check(st, "sdpa_dropout_mask_debug")
+    return mask
+
+
+def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deterministic=False):
+    """sdpa_options (by pointer) for the *_ex calls; rng_state is a device
+    tensor holding {seed, offset} as two 64-bit integers, or None."""
+    o = SdpaOptions()
+    if rng_state is not None:
+        if not rng_state.is_cuda or rng_state.numel() < 2 or rng_state.element_size() != 8:
+            raise ValueError("rng_state must be a CUDA tensor of two 64-bit integers {seed, offset}")
+        o.rng_state = rng_state.data_ptr()
+    o.batch_offset = int(batch_offset)
+    o.head_offset = int(head_offset)
+    o.total_heads = int(total_heads)
+    o.deterministic = int(bool(deterministic))
+    return o
+
+
+def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset=0,
+                rng_state=None, batch_offset=0, head_offset=0, total_heads=0, out=None, lse=None):
+    """Forward with options: ``rng_state`` (device {seed, offset}, read by the
+    kernels when they run, e.g. inside a replayed CUDA graph) and the batch /
+    head position of this call in a larger split problem. Returns (out, lse)."""
+    import torch
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    B, H, Sq, D = q.shape
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
+    opt = _options(rng_state, batch_offset, head_offset, total_heads)
+    dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(out)
+    st = lib.sdpa_fwd_ex(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), float(dropout_p),
+                         int(bool(is_causal)), _default_scale(D, scale), int(seed), int(offset),
+                         ctypes.byref(do_), ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                         ctypes.byref(opt), _stream(q.device))
+    _check(st, "sdpa_fwd_ex")
+    return out, lse
+
+
+def sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, deterministic=False):
+    opt = _options(deterministic=deterministic)
+    return int(load_library().sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))
+
+
+def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
+                scale=None, rng_state=None, batch_offset=0, head_offset=0, total_heads=0,
+                deterministic=False, dq=None, dk=None, dv=None, workspace=None):
+    """Backward with options (see :func:`sdpa_fwd_ex`); ``deterministic``
+    selects the fixed-order dQ accumulation. Returns (dq, dk, dv)."""
+    import torch
+    lib = load_library()
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_tensor(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic)
+    need = int(lib.sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    descs = [_desc(t) for t in (dout, q, k, v, out, dq, dk, dv)]
+    refs = [ctypes.byref(d) for d in descs]
+    st = lib.sdpa_bwd_ex(refs[0], refs[1], refs[2], refs[3], refs[4],
+                         ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                         float(dropout_p), int(bool(is_causal)), int(seed), int(offset),
+                         _default_scale(D, scale), refs[5], refs[6], refs[7],
+                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                         ctypes.byref(opt), _stream(q.device))
+    _check(st, "sdpa_bwd_ex")
+    return dq, dk, dv
+
+
+def sdpa_dropout_mask_debug_ex(B, H, Sq, Sk, dropout_p, seed=0, offset=0, rng_state=None,
+                               batch_offset=0, head_offset=0, total_heads=0, device="cuda"):
+    """Keep mask [B,H,Sq,Sk] of a block at (batch_offset, head_offset) of a
+    problem with total_heads heads, optionally keyed from device memory."""
+    import torch
+    lib = load_library()
+    mask = torch.empty((B, H, Sq, Sk), dtype=torch.uint8, device=device)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads)
+    st = lib.sdpa_dropout_mask_debug_ex(B, H, Sq, Sk, float(dropout_p), int(seed), int(offset),
+                                        ctypes.byref(opt),
+                                        ctypes.c_void_p(mask.data_ptr() if mask.numel() else None),
+                                        _stream(mask.device))
+    _check(st, "sdpa_dropout_mask_debug_ex")
     return mask
 
 

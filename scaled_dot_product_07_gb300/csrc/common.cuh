@@ -2,6 +2,7 @@
 // their host-side launchers.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -32,6 +33,8 @@ struct FwdParams {
   uint32_t drop_threshold;  // floor(p * 2^32)
   float drop_rescale;       // 1 / (1 - p)
   PhiloxKey pk;
+  const uint64_t* rng_dev;  // device {seed, offset} overriding pk, or null
+  int b0, h0, H_total;      // counter position of this launch in the whole problem
   float* lse;             // [B, H, Sq] fp32
   uint32_t* err;          // device error word
   uint64_t wait_limit_ns;
@@ -45,7 +48,11 @@ struct BwdParams {
   uint32_t drop_threshold;
   float drop_rescale;
   PhiloxKey pk;
-  float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32
+  const uint64_t* rng_dev;
+  int b0, h0, H_total;
+  float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
+  float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
+  size_t part_stride;     // one plain-stored partial per key tile (floats per slice)
   const float* lse2;      // workspace [B*H, Sq_pad]: lse * log2(e), +inf past Sq
   const float* delta;     // workspace [B*H, Sq_pad]: rowsum(dO * O), 0 past Sq
   uint32_t* err;
@@ -64,7 +71,7 @@ struct PreParams {
   const float* lse;       // [B,H,Sq]
   float* lse2;
   float* delta;
-  float* dq_acc;
+  float* dq_acc;          // zeroed here; null when the dQ partials are stored instead
 };
 
 struct ConvParams {
@@ -74,10 +81,39 @@ struct ConvParams {
   StridedBf16 dq;
 };
 
+// Deterministic dQ: dq = scale * sum over the key tiles that see the row, in
+// key-tile order, of the stored partials.
+struct SumParams {
+  int B, H, Sq, Sq_pad, D;
+  int n_kv_tiles;
+  int causal;
+  float scale;
+  const float* dq_part;
+  size_t part_stride;
+  StridedBf16 dq;
+};
+
+// Opt the kernel into `bytes` of dynamic shared memory, once per device: later
+// launches (including those recorded while a stream is being captured into a
+// CUDA graph) then make no call besides the launch itself.
+template <auto Kern>
+cudaError_t ensure_smem_attr(int bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 // Launchers (defined in the .cu files). Each returns the launch's CUDA error.
 cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps /*q,k,v,o*/,
                        const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout,
                             const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
                             cudaStream_t stream);

@@ -74,6 +74,29 @@ __device__ __forceinline__ void keep_bits(uint64_t n0, uint32_t threshold, const
   for (int i = 0; i < W; ++i) bits[i] = __funnelshift_r(s[i], s[i + 1], a);
 }
 
+// The key of one launch: the one passed in the kernel parameters, or, when
+// the caller handed over a device pointer to {seed, offset} (so that a
+// captured graph can be replayed with fresh values), the one read from it.
+__device__ __forceinline__ PhiloxKey launch_key(const PhiloxKey& pk, const uint64_t* rng_dev) {
+  if (rng_dev == nullptr) return pk;
+  const uint64_t seed = rng_dev[0], off = rng_dev[1];
+  PhiloxKey k;
+  k.k0 = static_cast<uint32_t>(seed);
+  k.k1 = static_cast<uint32_t>(seed >> 32);
+  k.off_lo = static_cast<uint32_t>(off);
+  k.off_hi = static_cast<uint32_t>(off >> 32);
+  return k;
+}
+
+// Flat (batch, head) index of the counter: b*H + h over the whole problem,
+// so a launch that holds a slice of the batches and heads (b0, h0 its first
+// ones, H_total the problem's heads per batch) draws the slice of the whole
+// problem's mask.
+__device__ __forceinline__ uint64_t counter_bh(int b, int h, int b0, int h0, int H_total) {
+  return static_cast<uint64_t>(b0 + b) * static_cast<uint64_t>(H_total) +
+         static_cast<uint64_t>(h0 + h);
+}
+
 // Keep bit of one absolute index.
 __device__ __forceinline__ bool keep_one(uint64_t n, uint32_t threshold, const PhiloxKey& pk) {
   const uint4 u = philox_group(n >> 2, pk);

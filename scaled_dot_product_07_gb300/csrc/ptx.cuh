@@ -186,6 +186,23 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* dst, const void* src, 
       : "memory");
 }
 
+// Plain bulk copy shared -> global (bulk-group completion).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+// The step's dQ partial: reduce-added into the shared fp32 accumulator, or,
+// in deterministic mode, stored into this key tile's own slice.
+__device__ __forceinline__ void dq_out(float* acc, float* part_slice, size_t row_off, const void* src,
+                                       uint32_t bytes) {
+  if (part_slice != nullptr)
+    bulk_store(part_slice + row_off, src, bytes);
+  else
+    bulk_reduce_add_f32(acc + row_off, src, bytes);
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

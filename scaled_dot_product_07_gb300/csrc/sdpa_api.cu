@@ -17,11 +17,22 @@ __device__ uint32_t g_wait_error;
 
 // ------------------------------------------------------------ small kernels
 
-__global__ void __launch_bounds__(256) dropout_mask_kernel(int64_t total, uint32_t threshold,
-                                                           PhiloxKey pk, uint8_t* mask) {
+// Keep mask of a [B, H, Sq, Sk] block whose batches and heads start at
+// (b0, h0) of a problem with H_total heads per batch.
+__global__ void __launch_bounds__(256) dropout_mask_kernel(int64_t total, int64_t per_head, int H,
+                                                           int b0, int h0, int H_total,
+                                                           uint32_t threshold, PhiloxKey pk_arg,
+                                                           const uint64_t* rng_dev, uint8_t* mask) {
+  const PhiloxKey pk = launch_key(pk_arg, rng_dev);
   for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < total;
-       n += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    mask[n] = keep_one(static_cast<uint64_t>(n), threshold, pk) ? 1 : 0;
+       n += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t bh = n / per_head;
+    const int b = static_cast<int>(bh / H);
+    const int h = static_cast<int>(bh - static_cast<int64_t>(b) * H);
+    const uint64_t g = counter_bh(b, h, b0, h0, H_total) * static_cast<uint64_t>(per_head) +
+                       static_cast<uint64_t>(n - bh * per_head);
+    mask[n] = keep_one(g, threshold, pk) ? 1 : 0;
+  }
 }
 
 __global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
@@ -177,6 +188,39 @@ StridedBf16 strided(const sdpa_tensor* t) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Resolved sdpa_options.
+struct Opts {
+  const uint64_t* rng = nullptr;
+  int b0 = 0, h0 = 0, H_total = 0;
+  bool det = false;
+};
+
+sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                            Opts* r) {
+  Opts x;
+  x.H_total = static_cast<int>(H);
+  if (o) {
+    if (o->batch_offset < 0 || o->head_offset < 0 || o->total_heads < 0)
+      return SDPA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(o->rng_state) & 7u) return SDPA_ERR_ALIGNMENT;
+    const int64_t Ht = o->total_heads ? o->total_heads : H;
+    if (o->head_offset + H > Ht) return SDPA_ERR_INVALID_ARG;
+    const int64_t kMaxInt = 0x7fffffff;
+    if (o->batch_offset + B > kMaxInt || Ht > kMaxInt) return SDPA_ERR_INVALID_ARG;
+    // the global counter ((b*H_total + h)*Sq + i)*Sk + j must fit in 64 bits
+    const double n_max = static_cast<double>(o->batch_offset + B) * static_cast<double>(Ht) *
+                         static_cast<double>(Sq) * static_cast<double>(Sk);
+    if (n_max >= 1.8e19) return SDPA_ERR_INVALID_ARG;
+    x.rng = o->rng_state;
+    x.b0 = static_cast<int>(o->batch_offset);
+    x.h0 = static_cast<int>(o->head_offset);
+    x.H_total = static_cast<int>(Ht);
+    x.det = o->deterministic != 0;
+  }
+  *r = x;
+  return SDPA_OK;
+}
+
 sdpa_status finish(cudaError_t e, cudaStream_t stream) {
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
   if (debug_sync()) return sdpa_check_device(reinterpret_cast<sdpa_stream_t>(stream));
@@ -190,9 +234,10 @@ using namespace sdpa;
 
 extern "C" {
 
-sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
-                     double dropout_p, int is_causal, float scale, uint64_t seed,
-                     uint64_t offset, sdpa_tensor* out, float* lse, sdpa_stream_t stream_) {
+sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                        double dropout_p, int is_causal, float scale, uint64_t seed,
+                        uint64_t offset, sdpa_tensor* out, float* lse,
+                        const sdpa_options* options, sdpa_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   sdpa_status s = check_dims(q, k, v);
   if (s != SDPA_OK) return s;
@@ -206,6 +251,8 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
   if (B * H * Sq == 0) return SDPA_OK;
   if (Sk == 0) return SDPA_ERR_INVALID_ARG;  // softmax over no keys
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+  Opts opt;
+  if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
 
   CUtensorMap maps[4];
   if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
@@ -221,12 +268,23 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
   p.drop_threshold = drop_threshold(dropout_p);
   p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
   p.pk = philox_key(seed, offset);
+  p.rng_dev = opt.rng;
+  p.b0 = opt.b0;
+  p.h0 = opt.h0;
+  p.H_total = opt.H_total;
   p.lse = lse;
   p.err = error_word();
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return SDPA_ERR_CUDA;
   const bool dropout = dropout_p > 0.0;
   return finish(launch_fwd(static_cast<int>(D), is_causal != 0, dropout, maps, p, stream), stream);
+}
+
+sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                     double dropout_p, int is_causal, float scale, uint64_t seed,
+                     uint64_t offset, sdpa_tensor* out, float* lse, sdpa_stream_t stream) {
+  return sdpa_fwd_ex(q, k, v, dropout_p, is_causal, scale, seed, offset, out, lse, nullptr,
+                     stream);
 }
 
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D) {
@@ -236,11 +294,21 @@ size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int
   return static_cast<size_t>(B * H * Sq_pad * (D + 2) * 4);
 }
 
-sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
-                     const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
-                     double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
-                     float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
-                     void* workspace, size_t workspace_bytes, sdpa_stream_t stream_) {
+size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
+                                  const sdpa_options* options) {
+  if (!options || !options->deterministic) return sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
+  if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
+  const int64_t Sq_pad = round_up(Sq, 128);
+  const int64_t n_kv = (Sk + 127) / 128;
+  return static_cast<size_t>(B * H * Sq_pad * (D * n_kv + 2) * 4);
+}
+
+sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                        const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                        double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                        float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                        void* workspace, size_t workspace_bytes, const sdpa_options* options,
+                        sdpa_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   sdpa_status s = check_dims(q, k, v);
   if (s != SDPA_OK) return s;
@@ -264,14 +332,20 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
   }
   if (Sk == 0) return SDPA_ERR_INVALID_ARG;
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
-  const size_t need = sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
+  Opts opt;
+  if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
+  const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SDPA_ERR_WORKSPACE;
 
+  // workspace: [dQ accumulator | per-key-tile dQ partials (deterministic)], lse2, delta
   const int64_t Sq_pad = round_up(Sq, 128);
-  float* dq_acc = static_cast<float*>(workspace);
-  float* lse2 = dq_acc + B * H * Sq_pad * D;
+  const int64_t n_kv = (Sk + 127) / 128;
+  const int64_t slice = B * H * Sq_pad * D;
+  float* dq_region = static_cast<float*>(workspace);
+  float* lse2 = dq_region + slice * (opt.det ? n_kv : 1);
   float* delta = lse2 + B * H * Sq_pad;
+  float* dq_acc = opt.det ? nullptr : dq_region;
 
   const uint32_t mq = static_cast<uint32_t>(8192 / D);
   CUtensorMap maps[6];
@@ -309,7 +383,13 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
   p.drop_threshold = drop_threshold(dropout_p);
   p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
   p.pk = philox_key(seed, offset);
+  p.rng_dev = opt.rng;
+  p.b0 = opt.b0;
+  p.h0 = opt.h0;
+  p.H_total = opt.H_total;
   p.dq_acc = dq_acc;
+  p.dq_part = opt.det ? dq_region : nullptr;
+  p.part_stride = static_cast<size_t>(slice);
   p.lse2 = lse2;
   p.delta = delta;
   p.err = err;
@@ -317,6 +397,21 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
   e = launch_bwd_main(static_cast<int>(D), is_causal != 0, dropout_p > 0.0, maps, p, stream);
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
 
+  if (opt.det) {
+    SumParams sp;
+    sp.B = pp.B;
+    sp.H = pp.H;
+    sp.Sq = pp.Sq;
+    sp.Sq_pad = pp.Sq_pad;
+    sp.D = pp.D;
+    sp.n_kv_tiles = p.n_kv_tiles;
+    sp.causal = is_causal != 0;
+    sp.scale = scale;
+    sp.dq_part = dq_region;
+    sp.part_stride = static_cast<size_t>(slice);
+    sp.dq = strided(dq);
+    return finish(launch_bwd_dq_sum(sp, stream), stream);
+  }
   ConvParams cp;
   cp.B = pp.B;
   cp.H = pp.H;
@@ -329,20 +424,41 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
   return finish(launch_bwd_dq_convert(cp, stream), stream);
 }
 
-sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
-                                    double dropout_p, uint64_t seed, uint64_t offset,
-                                    uint8_t* mask, sdpa_stream_t stream_) {
+sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                     const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                     double dropout_p, int is_causal, uint64_t seed, uint64_t offset,
+                     float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv,
+                     void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
+  return sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p, is_causal, seed, offset, scale, dq, dk,
+                     dv, workspace, workspace_bytes, nullptr, stream);
+}
+
+sdpa_status sdpa_dropout_mask_debug_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                       double dropout_p, uint64_t seed, uint64_t offset,
+                                       const sdpa_options* options, uint8_t* mask,
+                                       sdpa_stream_t stream_) {
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return SDPA_ERR_INVALID_ARG;
   if (!(dropout_p >= 0.0 && dropout_p < 1.0)) return SDPA_ERR_INVALID_ARG;
   const int64_t total = B * H * Sq * Sk;
   if (total == 0) return SDPA_OK;
   if (!mask) return SDPA_ERR_INVALID_ARG;
+  if (H > 0x7fffffff) return SDPA_ERR_INVALID_ARG;
+  Opts opt;
+  const sdpa_status s = resolve_options(options, B, H, Sq, Sk, &opt);
+  if (s != SDPA_OK) return s;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const int64_t blocks = (total + 255) / 256;
   const unsigned grid = static_cast<unsigned>(blocks > 152 * 32 ? 152 * 32 : blocks);
-  dropout_mask_kernel<<<grid, 256, 0, stream>>>(total, drop_threshold(dropout_p),
-                                                philox_key(seed, offset), mask);
+  dropout_mask_kernel<<<grid, 256, 0, stream>>>(total, Sq * Sk, static_cast<int>(H), opt.b0,
+                                                opt.h0, opt.H_total, drop_threshold(dropout_p),
+                                                philox_key(seed, offset), opt.rng, mask);
   return finish(cudaGetLastError(), stream);
+}
+
+sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                                    double dropout_p, uint64_t seed, uint64_t offset,
+                                    uint8_t* mask, sdpa_stream_t stream) {
+  return sdpa_dropout_mask_debug_ex(B, H, Sq, Sk, dropout_p, seed, offset, nullptr, mask, stream);
 }
 
 sdpa_status sdpa_check_device(sdpa_stream_t stream_) {

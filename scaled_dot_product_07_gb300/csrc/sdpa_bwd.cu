@@ -56,9 +56,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const PreParams p) 
     }
     // groups of tpr consecutive lanes hold one row
     for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + row * p.D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.dq_acc != nullptr) {
+      float4* z = reinterpret_cast<float4*>(p.dq_acc + row * p.D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (part == 0) {
       p.delta[row] = acc;
       p.lse2[row] = i < p.Sq ? p.lse[bh * p.Sq + i] * kLog2e : INFINITY;
@@ -87,6 +89,41 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p)
     o.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
     o.z = pack_bf16x2(c.x * p.scale, c.y * p.scale);
     o.w = pack_bf16x2(c.z * p.scale, c.w * p.scale);
+    const int64_t e = b * p.dq.sB + h * p.dq.sH + i * p.dq.sS + part * 8;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq.data) + e) = o;
+  }
+}
+
+// ---------------------------------------------------------------- deterministic dQ sum
+
+// Key tile k stores a partial for every query row r >= 128 k (causal, top-left;
+// every row otherwise): the sum runs over exactly those tiles, in tile order,
+// so the result does not depend on the order in which the CTAs finished.
+__global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
+  const int cpr = p.D / 8;
+  const int64_t total = static_cast<int64_t>(p.B) * p.H * p.Sq * cpr;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = idx / cpr;
+    const int part = static_cast<int>(idx - row * cpr);
+    const int64_t bh = row / p.Sq;
+    const int i = static_cast<int>(row - bh * p.Sq);
+    const int b = static_cast<int>(bh / p.H);
+    const int h = static_cast<int>(bh - static_cast<int64_t>(b) * p.H);
+    const int k_last = p.causal ? min(p.n_kv_tiles - 1, i / 128) : p.n_kv_tiles - 1;
+    const float* src = p.dq_part + (bh * p.Sq_pad + i) * p.D + part * 8;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k <= k_last; ++k) {
+      const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(k) * p.part_stride);
+      const float4 x = s4[0], y = s4[1];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(a[0] * p.scale, a[1] * p.scale);
+    o.y = pack_bf16x2(a[2] * p.scale, a[3] * p.scale);
+    o.z = pack_bf16x2(a[4] * p.scale, a[5] * p.scale);
+    o.w = pack_bf16x2(a[6] * p.scale, a[7] * p.scale);
     const int64_t e = b * p.dq.sB + h * p.dq.sH + i * p.dq.sS + part * 8;
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq.data) + e) = o;
   }
@@ -390,6 +427,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + L::kTmemS + lane_base, tDP = tmem + L::kTmemDP + lane_base;
     const uint32_t pa = sb + L::kPt, da = sb + L::kDst;
+    const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
     for (int t = 0; t < n_steps; ++t) {
       const int st = t % S;
       const int i0 = (qt_first + t) * MQ;
@@ -413,10 +451,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int w = 0; w < MQ / 32; ++w) kb[w] = 0xffffffffu;
       if (DROPOUT) {
-        const uint64_t n_base = (static_cast<uint64_t>(bh) * p.Sq + i0) * static_cast<uint64_t>(p.Sk) + kj;
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + i0) *
+                                    static_cast<uint64_t>(p.Sk) +
+                                kj;
 #pragma unroll
         for (int c = 0; c < MQ; ++c) {
-          const bool kp = keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, p.pk);
+          const bool kp = keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, pk);
           if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
         }
       }
@@ -469,6 +509,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
     const uint32_t tDQ = tmem + L::kTmemDQ + lane_base;
     const uint32_t qa = sb + L::kDq;
+    float* part = p.dq_part ? p.dq_part + static_cast<size_t>(kv_tile) * p.part_stride : nullptr;
     for (int t = 0; t < n_steps; ++t) {
       const int i0 = (qt_first + t) * MQ;
       mbar_wait(dq_full, t & 1, wc, kSiteBwdDqFull);
@@ -507,8 +548,8 @@ __global__ void __launch_bounds__(320, 1)
       fence_async_smem();
       named_barrier_sync(2, 128);
       if (lt == 0) {
-        bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + i0) * D,
-                            smem + L::kDq, L::kDqBytes);
+        dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0) * D, smem + L::kDq,
+               L::kDqBytes);
         bulk_commit();
       }
     }
@@ -575,7 +616,7 @@ template <int D, bool C, bool DR>
 cudaError_t launch_bwd_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_main_kernel<D, C, DR>;
   const int smem = BwdLayout<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel<D, C, DR>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, 320, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
@@ -602,6 +643,12 @@ cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream) {
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D / 8);
   bwd_dq_convert_kernel<<<elementwise_grid(items), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream) {
+  const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D / 8);
+  bwd_dq_sum_kernel<<<elementwise_grid(items), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t tS = tmem + L::tmem_s(x) + lane_base;
     const uint32_t tDP = tmem + L::tmem_dp(x) + lane_base;
     const uint32_t da = sb + L::kDs + x * L::kDsBytes;
+    const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
     for (int t = x, k = 0; t < n_steps; t += 2, ++k) {
       const int st = t % NS;
       const int i0 = (qt_first + t) * MQ;
@@ -301,12 +302,13 @@ __global__ void __launch_bounds__(448, 1)
       }
       uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
       if (DROPOUT) {
-        const uint64_t n_base =
-            (static_cast<uint64_t>(bh) * p.Sq + i0) * static_cast<uint64_t>(p.Sk) + kj;
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + i0) *
+                                    static_cast<uint64_t>(p.Sk) +
+                                kj;
 #pragma unroll
         for (int c = 0; c < MQ; ++c) {
           const bool kp =
-              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, p.pk);
+              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, pk);
           if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
         }
       }
@@ -364,6 +366,7 @@ __global__ void __launch_bounds__(448, 1)
     const int lt = threadIdx.x - 256;  // TMEM lane = d
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t qa = sb + L::kDq;
+    float* part = p.dq_part ? p.dq_part + static_cast<size_t>(kv_tile) * p.part_stride : nullptr;
     for (int t = 0; t < n_steps; ++t) {
       const int x = t & 1;
       const int i0 = (qt_first + t) * MQ;
@@ -387,8 +390,8 @@ __global__ void __launch_bounds__(448, 1)
       fence_async_smem();
       named_barrier_sync(2, 128);
       if (lt == 0) {
-        bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.Sq_pad + i0) * 128,
-                            smem + L::kDq, L::kDqBytes);
+        dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0) * 128, smem + L::kDq,
+               L::kDqBytes);
         bulk_commit();
       }
     }
@@ -454,7 +457,7 @@ template <bool C, bool DR>
 cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_main_kernel_d128<C, DR>;
   const int smem = B128::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, B128::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);

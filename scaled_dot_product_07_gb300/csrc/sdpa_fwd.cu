@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t pair_bar = 1 + (warp & 3);  // + 4 * tile
     float* red = reinterpret_cast<float*>(smem + L::kRed);
     const float sl2 = p.scale_log2;
+    const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
     float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
     float l[2] = {0.f, 0.f};              // this half's running sum, per tile
     // the half's tile max, shared with the partner half; returns the row's tile max
@@ -330,9 +331,9 @@ __global__ void __launch_bounds__(320, 1)
 
         uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
         if (DROPOUT) {
-          const uint64_t n_row =
-              (static_cast<uint64_t>(bh) * p.Sq + qi) * static_cast<uint64_t>(p.Sk);
-          keep_bits<2>(n_row + k0, p.drop_threshold, p.pk, keep);
+          const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + qi) *
+                                 static_cast<uint64_t>(p.Sk);
+          keep_bits<2>(n_row + k0, p.drop_threshold, pk, keep);
         }
         float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
         uint32_t pk2[32];
@@ -422,7 +423,7 @@ template <int D, bool C, bool DR>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
   auto kern = fwd_kernel<D, C, DR>;
   const int smem = FwdLayout<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);

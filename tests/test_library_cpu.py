@@ -163,3 +163,56 @@ def test_noalloc_backward_rejects_oversize_problems_on_the_host(lib):
     st = lib.sdpa_bwd_noalloc(r(t), r(t), r(t), r(t), r(t), ctypes.c_void_p(FAKE), 0.0, 1, 0, 0,
                               0.1, r(t), r(t), r(t), None)
     assert st == 6
+
+
+def options(**kw):
+    import scaled_dot_product_07_gb300 as sdpa
+    o = sdpa.SdpaOptions()
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o
+
+
+def test_deterministic_workspace_holds_one_dq_slice_per_key_tile(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    # one fp32 [B*H, ceil128(Sq), D] slice per 128-key tile, plus lse2 and delta
+    assert sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, True) == 2 * 3 * 256 * (64 * 3 + 2) * 4
+    assert (sdpa.sdpa_bwd_workspace_size_ex(8, 16, 4096, 4096, 128, True)
+            == 8 * 16 * 4096 * (128 * 32 + 2) * 4)
+    # without the flag (or with no options at all) it is the plain workspace
+    assert (sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, False)
+            == sdpa.sdpa_bwd_workspace_size(2, 3, 200, 300, 64))
+    assert lib.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, None) == lib.sdpa_bwd_workspace_size(
+        2, 3, 200, 300, 64)
+
+
+def test_option_errors_are_reported_before_any_launch(lib):
+    B, H, S, D = 2, 4, 300, 64  # three key tiles
+    t = desc(B, H, S, D)
+    r = ctypes.byref
+
+    def fwd(o):
+        return lib.sdpa_fwd_ex(r(t), r(t), r(t), 0.1, 1, 0.125, 1, 0, r(t), ctypes.c_void_p(FAKE),
+                               r(o), None)
+
+    # head slice past the problem's heads; negative offsets; misaligned rng pointer
+    assert fwd(options(head_offset=1)) == 1                       # total_heads 0 means H
+    assert fwd(options(head_offset=3, total_heads=6)) == 1       # 3 + 4 > 6
+    assert fwd(options(batch_offset=-1)) == 1
+    assert fwd(options(total_heads=-2)) == 1
+    assert fwd(options(rng_state=FAKE + 4)) == 3
+    # the global counter must fit in 64 bits
+    assert fwd(options(batch_offset=2**30, total_heads=2**30)) == 1
+
+    def bwd(o, ws_bytes):
+        return lib.sdpa_bwd_ex(r(t), r(t), r(t), r(t), r(t), ctypes.c_void_p(FAKE), 0.0, 1, 0, 0,
+                               0.125, r(t), r(t), r(t), ctypes.c_void_p(FAKE), ws_bytes, r(o), None)
+
+    # deterministic mode needs its larger workspace
+    plain = lib.sdpa_bwd_workspace_size(B, H, S, S, D)
+    det = lib.sdpa_bwd_workspace_size_ex(B, H, S, S, D, r(options(deterministic=1)))
+    assert det > plain
+    assert bwd(options(deterministic=1), det - 1) == 6
+    assert bwd(options(head_offset=2, total_heads=5), plain) == 1
+    assert lib.sdpa_dropout_mask_debug_ex(B, H, S, S, 0.1, 0, 0, r(options(head_offset=9)),
+                                          ctypes.c_void_p(FAKE), None) == 1

@@ -87,7 +87,7 @@ def test_workload_parity(cuda_lib, name, layout):
 
 
 # shapes that span several tiles and leave ragged tails on both axes
-RAGGED = [(200, 200), (77, 333), (333, 77), (1, 1), (129, 257), (256, 128), (1, 300)]
+RAGGED = [(200, 200), (77, 333), (333, 77), (1, 1), (129, 257), (256, 128), (1, 300), (333, 460)]
 
 
 @pytest.mark.parametrize("D", [64, 128])
