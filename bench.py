@@ -18,7 +18,8 @@ roofline    the backward (dominant) and forward kernels against the measured
             dense bf16 peak.
 extended    the options entry points on the same workload: the step recorded
             once as a CUDA graph (rng state read from device memory) and
-            replayed, and the deterministic (fixed-order dQ) backward.
+            replayed, and the deterministic (fixed-order dQ) backward; and
+            the same shape at head dim 96.
 cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
             the same workload (whole heads), on this host's cores.
 """
@@ -366,6 +367,29 @@ def bench_ours(args, w):
             "ms": d_ms, "tflops": f_bwd / (d_ms * 1e-3) / 1e12, "workspace_bytes": ws_det.numel(),
             "note": "one fp32 dQ partial per 128-key tile, summed in key-tile order"}
         del ws_det
+        # a head dim the kernels are not built for (96: the 128-wide kernels
+        # with the last 32 columns zero-filled by TMA), same B, H, S
+        w96 = W.Workload(w.name + "_d96", w.B, w.H, w.Sq, w.Sk, 96, w.is_causal, w.dropout_p,
+                         seed=w.seed, offset=w.offset, input_seed=w.input_seed)
+        g96 = torch.Generator(device="cpu")
+        g96.manual_seed(w.input_seed)
+        q96, k96, v96, do96 = (torch.randn(x.shape[:3] + (96,), generator=g96).to(torch.bfloat16)
+                               .to(dev) for x in (q, k, v, do))
+        out96, lse96 = torch.empty_like(q96), torch.empty_like(lse)
+        dq96, dk96, dv96 = torch.empty_like(q96), torch.empty_like(k96), torch.empty_like(v96)
+        ws96 = torch.empty(sdpa.sdpa_bwd_workspace_size(w.B, w.H, w.Sq, w.Sk, 96),
+                           dtype=torch.uint8, device=dev)
+        f96, b96 = flops(w96)
+        fwd96 = timed(lambda: sdpa.sdpa_fwd(q96, k96, v96, w.dropout_p, w.is_causal, None, w.seed,
+                                            w.offset, out=out96, lse=lse96), 5)
+        bwd96 = timed(lambda: sdpa.sdpa_bwd(do96, q96, k96, v96, out96, lse96, w.dropout_p,
+                                            w.is_causal, w.seed, w.offset, None, dq=dq96, dk=dk96,
+                                            dv=dv96, workspace=ws96), 5)
+        extras["head_dim_96"] = {
+            "fwd_ms": fwd96, "fwd_tflops": f96 / (fwd96 * 1e-3) / 1e12,
+            "bwd_ms": bwd96, "bwd_tflops": b96 / (bwd96 * 1e-3) / 1e12,
+            "note": "algorithmic flops at D=96; runs the D=128 kernels on zero-padded tiles"}
+        del q96, k96, v96, do96, out96, dq96, dk96, dv96, ws96
         if sdpa.sdpa_check_device() != 0:
             raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
 

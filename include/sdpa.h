@@ -21,7 +21,10 @@
  *   (stride[3] == 1); BHSE (stride order 3,2,1,0) and BSHE (3,1,2,0) are the
  *   two layouts of test_sdpa_loop_split. Strides of dims of size > 1 must be
  *   multiples of 8 elements (16 bytes) and every base pointer 16-byte aligned.
- * - D (= E = Ev, the head dim of q, k and v) must be 64 or 128.
+ * - D (= E = Ev, the head dim of q, k and v) must be a multiple of 8 from 8
+ *   to 128. The kernels are built for 64 and 128; a smaller D runs the next
+ *   larger one, the missing columns being read as zeros by the TMA loads and
+ *   clipped from the TMA stores, so the results are those of D itself.
  * - Causal masking is top-left aligned: key j is visible to query i iff j <= i.
  * - Ownership: the caller allocates every input, output and workspace; the
  *   library allocates no device memory and keeps no per-call state. Work is
@@ -59,7 +62,7 @@ typedef struct {
 typedef enum {
   SDPA_OK = 0,
   SDPA_ERR_INVALID_ARG = 1,    /* shape mismatch, null pointer, p outside [0,1), bad scale */
-  SDPA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, D not innermost */
+  SDPA_ERR_UNSUPPORTED = 2,    /* D not a multiple of 8 in [8, 128], D not innermost */
   SDPA_ERR_ALIGNMENT = 3,      /* base or stride not 16-byte aligned */
   SDPA_ERR_CUDA = 4,           /* a CUDA launch or driver call failed */
   SDPA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up on a bounded wait */

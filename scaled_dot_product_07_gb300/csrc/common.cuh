@@ -65,8 +65,11 @@ struct StridedBf16 {
   int64_t sB, sH, sS;  // element strides (D is contiguous)
 };
 
+// D is the kernels' head dim (64 or 128: the width of the fp32 dQ rows);
+// D_io the caller's head dim (a multiple of 8, at most D), the width of the
+// rows read from out / dout and written to dq.
 struct PreParams {
-  int B, H, Sq, Sq_pad, D;
+  int B, H, Sq, Sq_pad, D, D_io;
   StridedBf16 out, dout;
   const float* lse;       // [B,H,Sq]
   float* lse2;
@@ -75,7 +78,7 @@ struct PreParams {
 };
 
 struct ConvParams {
-  int B, H, Sq, Sq_pad, D;
+  int B, H, Sq, Sq_pad, D, D_io;
   float scale;
   const float* dq_acc;
   StridedBf16 dq;
@@ -84,7 +87,7 @@ struct ConvParams {
 // Deterministic dQ: dq = scale * sum over the key tiles that see the row, in
 // key-tile order, of the stored partials.
 struct SumParams {
-  int B, H, Sq, Sq_pad, D;
+  int B, H, Sq, Sq_pad, D, D_io;
   int n_kv_tiles;
   int causal;
   float scale;

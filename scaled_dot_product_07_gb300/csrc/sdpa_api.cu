@@ -188,6 +188,15 @@ StridedBf16 strided(const sdpa_tensor* t) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Head dims served: multiples of 8 up to 128. The kernels are built for 64
+// and 128; a smaller D runs the next larger one, with the missing columns of
+// q, k, v, dout read as zeros by the TMA loads (out-of-bounds fill) and never
+// written by the TMA stores (out-of-bounds elements are clipped). Zero
+// columns add nothing to Q K^T, dO V^T or any product, so the results are
+// those of the unpadded problem.
+bool head_dim_supported(int64_t D) { return D >= 8 && D <= 128 && D % 8 == 0; }
+int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+
 // Resolved sdpa_options.
 struct Opts {
   const uint64_t* rng = nullptr;
@@ -243,7 +252,8 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   if (s != SDPA_OK) return s;
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
-  if (D != 64 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  const int64_t Dk = kernel_head_dim(D);
   if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
@@ -277,7 +287,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return SDPA_ERR_CUDA;
   const bool dropout = dropout_p > 0.0;
-  return finish(launch_fwd(static_cast<int>(D), is_causal != 0, dropout, maps, p, stream), stream);
+  return finish(launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream), stream);
 }
 
 sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
@@ -291,7 +301,7 @@ size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
   const int64_t Sq_pad = round_up(Sq, 128);
-  return static_cast<size_t>(B * H * Sq_pad * (D + 2) * 4);
+  return static_cast<size_t>(B * H * Sq_pad * (kernel_head_dim(D) + 2) * 4);
 }
 
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
@@ -300,7 +310,7 @@ size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
   const int64_t Sq_pad = round_up(Sq, 128);
   const int64_t n_kv = (Sk + 127) / 128;
-  return static_cast<size_t>(B * H * Sq_pad * (D * n_kv + 2) * 4);
+  return static_cast<size_t>(B * H * Sq_pad * (kernel_head_dim(D) * n_kv + 2) * 4);
 }
 
 sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
@@ -314,7 +324,8 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if (s != SDPA_OK) return s;
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
-  if (D != 64 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  const int64_t Dk = kernel_head_dim(D);
   if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
@@ -341,13 +352,13 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   // workspace: [dQ accumulator | per-key-tile dQ partials (deterministic)], lse2, delta
   const int64_t Sq_pad = round_up(Sq, 128);
   const int64_t n_kv = (Sk + 127) / 128;
-  const int64_t slice = B * H * Sq_pad * D;
+  const int64_t slice = B * H * Sq_pad * Dk;
   float* dq_region = static_cast<float*>(workspace);
   float* lse2 = dq_region + slice * (opt.det ? n_kv : 1);
   float* delta = lse2 + B * H * Sq_pad;
   float* dq_acc = opt.det ? nullptr : dq_region;
 
-  const uint32_t mq = static_cast<uint32_t>(8192 / D);
+  const uint32_t mq = static_cast<uint32_t>(8192 / Dk);
   CUtensorMap maps[6];
   if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
       !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
@@ -361,7 +372,8 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   pp.H = static_cast<int>(H);
   pp.Sq = static_cast<int>(Sq);
   pp.Sq_pad = static_cast<int>(Sq_pad);
-  pp.D = static_cast<int>(D);
+  pp.D = static_cast<int>(Dk);
+  pp.D_io = static_cast<int>(D);
   pp.out = strided(out);
   pp.dout = strided(dout);
   pp.lse = lse;
@@ -394,7 +406,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   p.delta = delta;
   p.err = err;
   p.wait_limit_ns = wait_limit_ns();
-  e = launch_bwd_main(static_cast<int>(D), is_causal != 0, dropout_p > 0.0, maps, p, stream);
+  e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
 
   if (opt.det) {
@@ -404,6 +416,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
     sp.Sq = pp.Sq;
     sp.Sq_pad = pp.Sq_pad;
     sp.D = pp.D;
+    sp.D_io = pp.D_io;
     sp.n_kv_tiles = p.n_kv_tiles;
     sp.causal = is_causal != 0;
     sp.scale = scale;
@@ -418,6 +431,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   cp.Sq = pp.Sq;
   cp.Sq_pad = pp.Sq_pad;
   cp.D = pp.D;
+  cp.D_io = pp.D_io;
   cp.scale = scale;
   cp.dq_acc = dq_acc;
   cp.dq = strided(dq);

@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const PreParams p) 
     const int b = static_cast<int>(bh / p.H);
     const int h = static_cast<int>(bh - static_cast<int64_t>(b) * p.H);
     float acc = 0.f;
-    if (i < p.Sq) {
+    if (i < p.Sq && part * 8 < p.D_io) {  // columns past D_io are the kernels' zero padding
       const int64_t eo = b * p.out.sB + h * p.out.sH + i * p.out.sS + part * 8;
       const int64_t ed = b * p.dout.sB + h * p.dout.sH + i * p.dout.sS + part * 8;
       const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.out.data) + eo);
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const PreParams p) 
 // ---------------------------------------------------------------- dQ convert
 
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p) {
-  const int cpr = p.D / 8;  // 8-element chunks per row
+  const int cpr = p.D_io / 8;  // 8-element chunks per output row
   const int64_t total = static_cast<int64_t>(p.B) * p.H * p.Sq * cpr;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p)
 // every row otherwise): the sum runs over exactly those tiles, in tile order,
 // so the result does not depend on the order in which the CTAs finished.
 __global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
-  const int cpr = p.D / 8;
+  const int cpr = p.D_io / 8;
   const int64_t total = static_cast<int64_t>(p.B) * p.H * p.Sq * cpr;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -641,13 +641,13 @@ cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream) {
-  const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D / 8);
+  const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D_io / 8);
   bwd_dq_convert_kernel<<<elementwise_grid(items), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream) {
-  const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D / 8);
+  const int64_t items = static_cast<int64_t>(p.B) * p.H * p.Sq * (p.D_io / 8);
   bwd_dq_sum_kernel<<<elementwise_grid(items), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -58,6 +58,9 @@ def test_workspace_size(lib):
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (64 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(8, 16, 4096, 4096, 128) == 8 * 16 * 4096 * 130 * 4
     assert sdpa.sdpa_bwd_workspace_size(0, 3, 200, 77, 64) == 0
+    # a head dim below 64 (128) uses the 64-wide (128-wide) accumulator rows
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (64 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 96) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(1, 1, 0, 77, 64) == 0
 
 
@@ -85,7 +88,10 @@ def fwd_status(lib, q, k, v, o, p=0.0, causal=0, scale=0.125, lse=FAKE):
 def test_forward_argument_errors(lib):
     B, H, S, D = 2, 3, 100, 64
     ok = lambda: desc(B, H, S, D)
-    assert fwd_status(lib, desc(B, H, S, 96), desc(B, H, S, 96), desc(B, H, S, 96), desc(B, H, S, 96)) == 2
+    # head dims: multiples of 8 up to 128
+    for bad in (100, 136, 4):
+        assert fwd_status(lib, desc(B, H, S, bad), desc(B, H, S, bad), desc(B, H, S, bad),
+                          desc(B, H, S, bad)) == 2
     # E != Ev
     assert fwd_status(lib, ok(), ok(), desc(B, H, S, 128), ok()) == 1
     # K and V disagree on Sk; batch mismatch

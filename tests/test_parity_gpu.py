@@ -204,3 +204,20 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     gpu = run_gpu(cuda_lib, w, inputs, "BHSE")
     ref = oracle_heads(w, inputs, sampled_heads(w))
     compare(gpu, ref, sampled_heads(w), "after-timeout")
+
+
+# head dims other than 64 and 128 (multiples of 8): the 64- or 128-wide
+# kernels with the missing columns zero-filled by TMA
+@pytest.mark.parametrize("D", [8, 32, 40, 72, 96, 120])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("p", [0.0, 0.15])
+def test_other_head_dims_parity(cuda_lib, D, causal, p):
+    Sq, Sk = 200, 330
+    w = W.Workload("headdim", 1, 3, Sq, Sk, D, causal, p, seed=5 + D, offset=D,
+                   input_seed=700 + D)
+    inputs = W.draw_inputs(w)
+    layout = "BSHE" if D in (40, 96) else "BHSE"
+    gpu = run_gpu(cuda_lib, w, inputs, layout)
+    heads = [(0, h) for h in range(w.H)]
+    ref = oracle_heads(w, inputs, heads)
+    compare(gpu, ref, heads, f"D{D} c{int(causal)} p{p} {layout}")
