@@ -33,6 +33,14 @@ What is computed, and where it comes from
   probabilities after the softmax: P~ = P * keep / (1 - p); the
   log-sum-exp is that of the undropped scores.
 
+* Additive attention bias: the forum thread asks for self-attention with
+  relative positional encoding through scaled_dot_product_attention, and
+  the priority-order discussion of PR 103704 mentions adding attn_bias
+  support to the memory-efficient kernel. It is read as torch's float
+  ``attn_mask``: a bias B_ij added to the scaled scores before the softmax,
+  ``S = scale * Q K^T + B`` (then the causal mask), and the log-sum-exp is
+  that of these biased scores. Its gradient is ``dB = dS``.
+
 Backward (the standard derivative of the forward above)::
 
     dV = P~^T dO
@@ -75,13 +83,16 @@ def _heads(B, H, heads):
     return [(b, h) for b in range(B) for h in range(H)] if heads is None else list(heads)
 
 
-def head_forward(qh, kh, vh, b, h, H, dropout_p, is_causal, scale, seed, offset):
-    """Forward of one head. qh [Sq,D], kh [Sk,D], vh [Sk,D] (float64).
+def head_forward(qh, kh, vh, b, h, H, dropout_p, is_causal, scale, seed, offset, bias=None):
+    """Forward of one head. qh [Sq,D], kh [Sk,D], vh [Sk,D] (float64);
+    bias: optional additive bias [Sq,Sk] of this head.
 
     Returns (out [Sq,D], lse [Sq]).
     """
     Sq, Sk = qh.shape[0], kh.shape[0]
     S = scale * (qh @ kh.T)
+    if bias is not None:
+        S = S + bias
     S = np.where(_visible(Sq, Sk, is_causal), S, -np.inf)
     m = S.max(axis=1, keepdims=True)
     lse = m[:, 0] + np.log(np.exp(S - m).sum(axis=1))
@@ -92,10 +103,13 @@ def head_forward(qh, kh, vh, b, h, H, dropout_p, is_causal, scale, seed, offset)
 
 
 def head_backward(doh, qh, kh, vh, outh, lseh, b, h, H, dropout_p, is_causal,
-                  scale, seed, offset, check_delta=True):
-    """Backward of one head; returns (dq [Sq,D], dk [Sk,D], dv [Sk,D])."""
+                  scale, seed, offset, check_delta=True, bias=None):
+    """Backward of one head; returns (dq [Sq,D], dk [Sk,D], dv [Sk,D]), and
+    dbias [Sq,Sk] as a fourth item when ``bias`` is given."""
     Sq, Sk = qh.shape[0], kh.shape[0]
     S = scale * (qh @ kh.T)
+    if bias is not None:
+        S = S + bias
     S = np.where(_visible(Sq, Sk, is_causal), S, -np.inf)
     P = np.exp(S - lseh[:, None])
     Z = _dropout_factor(b, h, H, Sq, Sk, dropout_p, seed, offset)
@@ -111,15 +125,26 @@ def head_backward(doh, qh, kh, vh, outh, lseh, b, h, H, dropout_p, is_causal,
     dS = P * (dP - delta[:, None])
     dq = scale * (dS @ kh)
     dk = scale * (dS.T @ qh)
+    if bias is not None:
+        return dq, dk, dv, dS
     return dq, dk, dv
 
 
+def _bias_of(bias, b, h):
+    """The [Sq,Sk] bias of head (b, h) from a [B or 1, H or 1, Sq, Sk] array."""
+    if bias is None:
+        return None
+    return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
+
+
 def sdpa_fwd(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset=0,
-             heads=None):
+             heads=None, bias=None):
     """Forward over logical [B,H,S,D] float64 arrays.
 
     ``heads``: optional iterable of (b, h) pairs; only those heads are
-    computed (the others are left NaN). Returns (out [B,H,Sq,D], lse [B,H,Sq]).
+    computed (the others are left NaN). ``bias``: optional additive bias
+    [B or 1, H or 1, Sq, Sk] (a size-1 dim is shared by every batch / head).
+    Returns (out [B,H,Sq,D], lse [B,H,Sq]).
     """
     q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
     B, H, Sq, D = q.shape
@@ -127,15 +152,20 @@ def sdpa_fwd(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset
         scale = default_scale(D)
     out = np.full((B, H, Sq, v.shape[3]), np.nan)
     lse = np.full((B, H, Sq), np.nan)
+    if bias is not None:
+        bias = np.asarray(bias, dtype=np.float64)
     for b, h in _heads(B, H, heads):
         out[b, h], lse[b, h] = head_forward(q[b, h], k[b, h], v[b, h], b, h, H,
-                                            dropout_p, is_causal, scale, seed, offset)
+                                            dropout_p, is_causal, scale, seed, offset,
+                                            bias=_bias_of(bias, b, h))
     return out, lse
 
 
 def sdpa_bwd(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
-             scale=None, heads=None, check_delta=True):
-    """Backward over logical [B,H,S,D] float64 arrays; returns (dq, dk, dv)."""
+             scale=None, heads=None, check_delta=True, bias=None):
+    """Backward over logical [B,H,S,D] float64 arrays; returns (dq, dk, dv),
+    and dbias [B,H,Sq,Sk] (per head, not summed over shared dims) as a
+    fourth item when ``bias`` is given."""
     dout, q, k, v, out, lse = (np.asarray(t, dtype=np.float64)
                                for t in (dout, q, k, v, out, lse))
     B, H, Sq, D = q.shape
@@ -144,8 +174,16 @@ def sdpa_bwd(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, of
     dq = np.full(q.shape, np.nan)
     dk = np.full(k.shape, np.nan)
     dv = np.full(v.shape, np.nan)
+    if bias is not None:
+        bias = np.asarray(bias, dtype=np.float64)
+        dbias = np.full((B, H, q.shape[2], k.shape[2]), np.nan)
     for b, h in _heads(B, H, heads):
-        dq[b, h], dk[b, h], dv[b, h] = head_backward(
-            dout[b, h], q[b, h], k[b, h], v[b, h], out[b, h], lse[b, h], b, h, H,
-            dropout_p, is_causal, scale, seed, offset, check_delta)
+        r = head_backward(dout[b, h], q[b, h], k[b, h], v[b, h], out[b, h], lse[b, h], b, h, H,
+                          dropout_p, is_causal, scale, seed, offset, check_delta,
+                          bias=_bias_of(bias, b, h))
+        dq[b, h], dk[b, h], dv[b, h] = r[:3]
+        if bias is not None:
+            dbias[b, h] = r[3]
+    if bias is not None:
+        return dq, dk, dv, dbias
     return dq, dk, dv

@@ -278,3 +278,93 @@ def test_head_subset_matches_full():
     o2, l2 = oracle.sdpa_fwd(q, k, v, 0.2, False, None, 1, 2, heads=[(1, 2)])
     np.testing.assert_array_equal(o2[1, 2], out[1, 2])
     assert np.isnan(o2[0, 0]).all()
+
+
+# ---------------------------------------------------------------- additive bias
+
+@pytest.mark.parametrize("causal,Sq,Sk,shared", [(False, 11, 11, False), (False, 7, 13, True),
+                                                 (True, 13, 9, False)])
+def test_bias_matches_torch_math_sdpa_fp64(causal, Sq, Sk, shared):
+    """Library special case: torch's CPU float64 SDPA with a float attn_mask,
+    and autograd for every gradient including the bias's (p = 0)."""
+    B, H, D, scale = 2, 3, 8, 0.3
+    q, k, v, do = (rnd((B, H, s, D), 60 + i) for i, s in enumerate((Sq, Sk, Sk, Sq)))
+    bias = rnd((1 if shared else B, H, Sq, Sk), 64)
+    out, lse = oracle.sdpa_fwd(q, k, v, 0.0, causal, scale, bias=bias)
+    tq, tk, tv, tb = (torch.tensor(x, requires_grad=True) for x in (q, k, v, bias))
+    mask = tb
+    if causal:
+        mask = tb.masked_fill(~torch.ones(Sq, Sk, dtype=torch.bool).tril(), float("-inf"))
+    tout = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(out, tout.detach().numpy(), atol=1e-12)
+    scores = scale * tq.detach() @ tk.detach().transpose(-1, -2) + mask.detach()
+    np.testing.assert_allclose(lse, torch.logsumexp(scores, dim=-1).numpy(), atol=1e-12)
+    tout.backward(torch.tensor(do))
+    dq, dk, dv, dbias = oracle.sdpa_bwd(do, q, k, v, out, lse, 0.0, causal, scale=scale, bias=bias)
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-11)
+    # the oracle returns the per-head dS; a shared bias's gradient is its sum
+    got = dbias.sum(axis=0, keepdims=True) if shared else dbias
+    np.testing.assert_allclose(got, tb.grad.numpy(), atol=1e-11)
+
+
+def test_row_constant_bias_only_shifts_lse():
+    """A bias constant along each row cancels in the softmax: out and every
+    input gradient are unchanged, lse moves by the constant, and each row of
+    dbias sums to zero."""
+    B, H, Sq, Sk, D = 1, 2, 6, 9, 4
+    q, k, v, do = rnd((B, H, Sq, D), 70), rnd((B, H, Sk, D), 71), rnd((B, H, Sk, D), 72), rnd((B, H, Sq, D), 73)
+    c = rnd((B, H, Sq, 1), 74) * 5
+    bias = np.broadcast_to(c, (B, H, Sq, Sk)).copy()
+    for causal, p in ((False, 0.0), (True, 0.3)):
+        out0, lse0 = oracle.sdpa_fwd(q, k, v, p, causal, None, 9, 1)
+        out1, lse1 = oracle.sdpa_fwd(q, k, v, p, causal, None, 9, 1, bias=bias)
+        np.testing.assert_allclose(out1, out0, atol=1e-12)
+        np.testing.assert_allclose(lse1, lse0 + c[..., 0], atol=1e-12)
+        g0 = oracle.sdpa_bwd(do, q, k, v, out0, lse0, p, causal, 9, 1)
+        g1 = oracle.sdpa_bwd(do, q, k, v, out1, lse1, p, causal, 9, 1, bias=bias)
+        for a, b in zip(g1[:3], g0):
+            np.testing.assert_allclose(a, b, atol=1e-12)
+        if p == 0.0:
+            np.testing.assert_allclose(g1[3].sum(axis=3), 0.0, atol=1e-12)
+
+
+def test_minus_infinity_bias_above_the_diagonal_is_the_causal_mask():
+    """The bias is added before the softmax: -inf above the diagonal gives
+    exactly the top-left causal result."""
+    B, H, S, D = 1, 2, 7, 3
+    q, k, v, do = (rnd((B, H, S, D), 80 + i) for i in range(4))
+    tri = np.where(np.tril(np.ones((S, S), dtype=bool)), 0.0, -np.inf)[None, None]
+    out_b, lse_b = oracle.sdpa_fwd(q, k, v, 0.2, False, None, 4, 0, bias=tri)
+    out_c, lse_c = oracle.sdpa_fwd(q, k, v, 0.2, True, None, 4, 0)
+    np.testing.assert_allclose(out_b, out_c, atol=1e-14)
+    np.testing.assert_allclose(lse_b, lse_c, atol=1e-14)
+    gb = oracle.sdpa_bwd(do, q, k, v, out_b, lse_b, 0.2, False, 4, 0, bias=tri)
+    gc = oracle.sdpa_bwd(do, q, k, v, out_c, lse_c, 0.2, True, 4, 0)
+    for a, b in zip(gb[:3], gc):
+        np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal,p", [(False, 0.0), (True, 0.3)])
+def test_bias_gradient_matches_central_differences(causal, p):
+    """dbias of L = sum(out * dO), the dropout mask held fixed by (seed, offset)."""
+    B, H, Sq, Sk, D = 1, 1, 5, 6, 3
+    seed, off, scale = 12, 3, 0.7
+    q, k, v, do = rnd((B, H, Sq, D), 90), rnd((B, H, Sk, D), 91), rnd((B, H, Sk, D), 92), rnd((B, H, Sq, D), 93)
+    bias = rnd((B, H, Sq, Sk), 94)
+    out, lse = oracle.sdpa_fwd(q, k, v, p, causal, scale, seed, off, bias=bias)
+    dbias = oracle.sdpa_bwd(do, q, k, v, out, lse, p, causal, seed, off, scale, bias=bias)[3]
+
+    def loss(bb):
+        return (oracle.sdpa_fwd(q, k, v, p, causal, scale, seed, off, bias=bb)[0] * do).sum()
+
+    eps = 1e-6
+    num = np.zeros_like(bias)
+    for idx in np.ndindex(*bias.shape):
+        a = bias.copy()
+        a[idx] += eps
+        lp = loss(a)
+        a[idx] -= 2 * eps
+        num[idx] = (lp - loss(a)) / (2 * eps)
+    np.testing.assert_allclose(dbias, num, atol=2e-7, rtol=1e-6)
