@@ -18,8 +18,9 @@ roofline    the backward (dominant) and forward kernels against the measured
             dense bf16 peak.
 extended    the options entry points on the same workload: the step recorded
             once as a CUDA graph (rng state read from device memory) and
-            replayed, and the deterministic (fixed-order dQ) backward; and
-            the same shape at head dim 96.
+            replayed, and the deterministic (fixed-order dQ) backward; the
+            same shape at head dim 96; and with an additive relative-position
+            bias (and its gradient).
 cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
             the same workload (whole heads), on this host's cores.
 """
@@ -390,6 +391,21 @@ def bench_ours(args, w):
             "bwd_ms": bwd96, "bwd_tflops": b96 / (bwd96 * 1e-3) / 1e12,
             "note": "algorithmic flops at D=96; runs the D=128 kernels on zero-padded tiles"}
         del q96, k96, v96, do96, out96, dq96, dk96, dv96, ws96
+        # additive bias: a relative-position bias shared by the batch, [1, H, Sq, Sk];
+        # the backward also writes its full [B, H, Sq, Sk] gradient
+        bias = W.padded_rows(W.draw_bias((1, w.H, w.Sq, w.Sk), w.input_seed + 17, "relpos").to(dev))
+        dbias = torch.empty((w.B, w.H, w.Sq, w.Sk), dtype=torch.bfloat16, device=dev)
+        fwd_b = timed(lambda: sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed,
+                                               w.offset, attn_bias=bias, out=out, lse=lse), 5)
+        bwd_b = timed(lambda: sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal,
+                                               w.seed, w.offset, attn_bias=bias, dbias=dbias,
+                                               dq=dq, dk=dk, dv=dv, workspace=ws), 5)
+        extras["attn_bias"] = {
+            "fwd_ms": fwd_b, "fwd_tflops": f_fwd / (fwd_b * 1e-3) / 1e12,
+            "bwd_ms": bwd_b, "bwd_tflops": f_bwd / (bwd_b * 1e-3) / 1e12,
+            "note": "bf16 relative-position bias [1,H,Sq,Sk] shared by the batch; the backward "
+                    "also writes dbias [B,H,Sq,Sk] bf16"}
+        del bias, dbias
         if sdpa.sdpa_check_device() != 0:
             raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
 

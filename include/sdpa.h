@@ -182,6 +182,20 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  *     total_heads heads per batch, so each part draws exactly its slice of
  *     the unsplit problem's mask. total_heads = 0 means H (no head split);
  *     otherwise head_offset + H <= total_heads. Offsets must be >= 0.
+ *   attn_bias: NULL, or an additive bias B_ij of the attention scores, for
+ *     example a relative-position bias (the forum thread's self-attention
+ *     with relative positional encoding; attn_bias in the memory-efficient
+ *     kernel, PR 103704's priority-order discussion). It is read as torch's
+ *     float attn_mask: softmax(scale * Q K^T + B + causal), and lse is that
+ *     of the biased scores. bfloat16, logical [B or 1, H or 1, Sq, Sk] (a
+ *     size-1 dim, or a stride-0 dim, is shared by every batch / head), keys
+ *     contiguous (stride[3] == 1), other strides multiples of 8 elements and
+ *     the base 16-byte aligned. Pass the same bias to sdpa_bwd_ex.
+ *   dbias: sdpa_bwd_ex only. NULL, or a bfloat16 [B, H, Sq, Sk] tensor
+ *     (keys contiguous) that receives dB = dS, the gradient of the loss with
+ *     respect to the biased scores, for every (b, h); positions hidden by
+ *     the causal mask get 0. Summing it over a shared dim gives the gradient
+ *     of a shared bias. Requires attn_bias.
  *   deterministic: sdpa_bwd_ex only. Nonzero: every 128-key tile stores its
  *     fp32 dQ partials into its own workspace slice and a final kernel adds
  *     them in key-tile order, so dq is bitwise reproducible run to run (the
@@ -196,6 +210,8 @@ typedef struct {
   int64_t head_offset;
   int64_t total_heads;
   int deterministic;
+  const sdpa_tensor* attn_bias;
+  sdpa_tensor* dbias;
 } sdpa_options;
 
 /* sdpa_fwd with options (NULL options = sdpa_fwd). */

@@ -66,7 +66,8 @@ class SdpaOptions(ctypes.Structure):
     """sdpa_options of include/sdpa.h."""
     _fields_ = [("rng_state", ctypes.c_void_p), ("batch_offset", ctypes.c_int64),
                 ("head_offset", ctypes.c_int64), ("total_heads", ctypes.c_int64),
-                ("deterministic", ctypes.c_int)]
+                ("deterministic", ctypes.c_int), ("attn_bias", ctypes.c_void_p),
+                ("dbias", ctypes.c_void_p)]
 
 
 def library_path():
@@ -256,10 +257,33 @@ def sdpa_dropout_mask_debug(B, H, Sq, Sk, dropout_p, seed, offset, device="cuda"
     return mask
 
 
-def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deterministic=False):
+def _bias_desc(t, name):
+    import torch
+    if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4:
+        raise ValueError(f"{name} must be a 4-D bfloat16 CUDA tensor [B or 1, H or 1, Sq, Sk]")
+    d = SdpaTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    for i in range(4):
+        d.size[i] = t.size(i)
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deterministic=False,
+             attn_bias=None, dbias=None):
     """sdpa_options (by pointer) for the *_ex calls; rng_state is a device
-    tensor holding {seed, offset} as two 64-bit integers, or None."""
+    tensor holding {seed, offset} as two 64-bit integers, or None; attn_bias
+    and dbias are bfloat16 tensors or None."""
     o = SdpaOptions()
+    o._keep = []
+    if attn_bias is not None:
+        bd = _bias_desc(attn_bias, "attn_bias")
+        o._keep.append(bd)
+        o.attn_bias = ctypes.addressof(bd)
+    if dbias is not None:
+        dd = _bias_desc(dbias, "dbias")
+        o._keep.append(dd)
+        o.dbias = ctypes.addressof(dd)
     if rng_state is not None:
         if not rng_state.is_cuda or rng_state.numel() < 2 or rng_state.element_size() != 8:
             raise ValueError("rng_state must be a CUDA tensor of two 64-bit integers {seed, offset}")
@@ -272,10 +296,13 @@ def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deter
 
 
 def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset=0,
-                rng_state=None, batch_offset=0, head_offset=0, total_heads=0, out=None, lse=None):
+                rng_state=None, batch_offset=0, head_offset=0, total_heads=0, attn_bias=None,
+                out=None, lse=None):
     """Forward with options: ``rng_state`` (device {seed, offset}, read by the
-    kernels when they run, e.g. inside a replayed CUDA graph) and the batch /
-    head position of this call in a larger split problem. Returns (out, lse)."""
+    kernels when they run, e.g. inside a replayed CUDA graph), the batch /
+    head position of this call in a larger split problem, and an additive
+    bfloat16 ``attn_bias`` [B or 1, H or 1, Sq, Sk] of the scaled scores.
+    Returns (out, lse)."""
     import torch
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -283,7 +310,7 @@ def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, off
     B, H, Sq, D = q.shape
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
-    opt = _options(rng_state, batch_offset, head_offset, total_heads)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads, attn_bias=attn_bias)
     dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.sdpa_fwd_ex(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), float(dropout_p),
                          int(bool(is_causal)), _default_scale(D, scale), int(seed), int(offset),
@@ -300,9 +327,12 @@ def sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, deterministic=False):
 
 def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
                 scale=None, rng_state=None, batch_offset=0, head_offset=0, total_heads=0,
-                deterministic=False, dq=None, dk=None, dv=None, workspace=None):
+                deterministic=False, attn_bias=None, dbias=None, dq=None, dk=None, dv=None,
+                workspace=None):
     """Backward with options (see :func:`sdpa_fwd_ex`); ``deterministic``
-    selects the fixed-order dQ accumulation. Returns (dq, dk, dv)."""
+    selects the fixed-order dQ accumulation. ``dbias``: None, True (allocate)
+    or a bfloat16 [B, H, Sq, Sk] tensor that receives the bias gradient dS.
+    Returns (dq, dk, dv), or (dq, dk, dv, dbias) when dbias is requested."""
     import torch
     lib = load_library()
     for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
@@ -312,7 +342,10 @@ def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic)
+    if dbias is True:
+        dbias = torch.empty((B, H, Sq, Sk), dtype=torch.bfloat16, device=q.device)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic, attn_bias,
+                   dbias)
     need = int(lib.sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
@@ -325,6 +358,8 @@ def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0,
                          ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
                          ctypes.byref(opt), _stream(q.device))
     _check(st, "sdpa_bwd_ex")
+    if dbias is not None:
+        return dq, dk, dv, dbias
     return dq, dk, dv
 
 

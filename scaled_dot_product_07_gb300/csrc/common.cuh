@@ -26,6 +26,23 @@ enum WaitSite : uint32_t {
   kSiteSelftest = 0x301,
 };
 
+// Additive attention bias: bf16 [B or 1, H or 1, Sq, Sk], keys contiguous;
+// a shared (size-1) batch or head dim has stride 0.
+struct AttnBias {
+  const uint16_t* data;       // bf16 bits; null: no bias
+  int64_t sB, sH, sS;         // element strides
+};
+
+// Gradient of the bias, bf16 [B, H, Sq, Sk], keys contiguous (null: not wanted).
+struct DBias {
+  uint16_t* data;
+  int64_t sB, sH, sS;
+};
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
 struct FwdParams {
   int B, H, Sq, Sk;
   int n_q_tiles;          // ceil(Sq / 256): pairs of 128-row query tiles per head
@@ -35,6 +52,8 @@ struct FwdParams {
   PhiloxKey pk;
   const uint64_t* rng_dev;  // device {seed, offset} overriding pk, or null
   int b0, h0, H_total;      // counter position of this launch in the whole problem
+  AttnBias bias;
+  float bias_to_raw;        // 1 / scale
   float* lse;             // [B, H, Sq] fp32
   uint32_t* err;          // device error word
   uint64_t wait_limit_ns;
@@ -50,6 +69,8 @@ struct BwdParams {
   PhiloxKey pk;
   const uint64_t* rng_dev;
   int b0, h0, H_total;
+  AttnBias bias;
+  DBias dbias;
   float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
   float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
   size_t part_stride;     // one plain-stored partial per key tile (floats per slice)
@@ -125,6 +146,10 @@ cudaError_t launch_bwd_main_d128(bool causal, bool dropout,
                                  cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStream_t stream);
+// Zeroes dbias(i, j) for j >= 128 * (i / 128 + 1): the key tiles a causal
+// backward never visits for row i.
+cudaError_t launch_dbias_zero_causal(const DBias& t, int B, int H, int Sq, int Sk,
+                                     cudaStream_t stream);
 cudaError_t launch_dropout_mask(int64_t B, int64_t H, int64_t Sq, int64_t Sk, uint32_t threshold,
                                 PhiloxKey pk, uint8_t* mask, cudaStream_t stream);
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);

@@ -203,6 +203,11 @@ __device__ __forceinline__ void dq_out(float* acc, float* part_slice, size_t row
     bulk_reduce_add_f32(acc + row_off, src, bytes);
 }
 
+// Start moving the line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

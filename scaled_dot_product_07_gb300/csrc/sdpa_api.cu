@@ -202,7 +202,41 @@ struct Opts {
   const uint64_t* rng = nullptr;
   int b0 = 0, h0 = 0, H_total = 0;
   bool det = false;
+  AttnBias bias{nullptr, 0, 0, 0};
+  DBias dbias{nullptr, 0, 0, 0};
 };
+
+sdpa_status check_bias(const sdpa_tensor* t, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                       AttnBias* out) {
+  if (!t->data) return SDPA_ERR_INVALID_ARG;
+  if ((t->size[0] != 1 && t->size[0] != B) || (t->size[1] != 1 && t->size[1] != H) ||
+      t->size[2] != Sq || t->size[3] != Sk)
+    return SDPA_ERR_INVALID_ARG;
+  for (int d = 0; d < 4; ++d)
+    if (t->stride[d] < 0) return SDPA_ERR_INVALID_ARG;
+  if (Sk > 1 && t->stride[3] != 1) return SDPA_ERR_UNSUPPORTED;
+  const int64_t sB = t->size[0] == 1 ? 0 : t->stride[0];
+  const int64_t sH = t->size[1] == 1 ? 0 : t->stride[1];
+  const int64_t sS = Sq == 1 ? 0 : t->stride[2];
+  // 16-byte vector loads of 8 keys
+  if ((reinterpret_cast<uintptr_t>(t->data) & 15u) || (sB % 8) || (sH % 8) || (sS % 8))
+    return SDPA_ERR_ALIGNMENT;
+  *out = AttnBias{static_cast<const uint16_t*>(t->data), sB, sH, sS};
+  return SDPA_OK;
+}
+
+sdpa_status check_dbias(const sdpa_tensor* t, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                        DBias* out) {
+  if (!t->data) return SDPA_ERR_INVALID_ARG;
+  if (t->size[0] != B || t->size[1] != H || t->size[2] != Sq || t->size[3] != Sk)
+    return SDPA_ERR_INVALID_ARG;
+  for (int d = 0; d < 4; ++d)
+    if (t->stride[d] < 0) return SDPA_ERR_INVALID_ARG;
+  if (Sk > 1 && t->stride[3] != 1) return SDPA_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(t->data) & 1u) return SDPA_ERR_ALIGNMENT;
+  *out = DBias{static_cast<uint16_t*>(t->data), t->stride[0], t->stride[1], t->stride[2]};
+  return SDPA_OK;
+}
 
 sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
                             Opts* r) {
@@ -220,6 +254,15 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
     const double n_max = static_cast<double>(o->batch_offset + B) * static_cast<double>(Ht) *
                          static_cast<double>(Sq) * static_cast<double>(Sk);
     if (n_max >= 1.8e19) return SDPA_ERR_INVALID_ARG;
+    if (o->attn_bias) {
+      const sdpa_status s = check_bias(o->attn_bias, B, H, Sq, Sk, &x.bias);
+      if (s != SDPA_OK) return s;
+    }
+    if (o->dbias) {
+      if (!o->attn_bias) return SDPA_ERR_INVALID_ARG;
+      const sdpa_status s = check_dbias(o->dbias, B, H, Sq, Sk, &x.dbias);
+      if (s != SDPA_OK) return s;
+    }
     x.rng = o->rng_state;
     x.b0 = static_cast<int>(o->batch_offset);
     x.h0 = static_cast<int>(o->head_offset);
@@ -282,6 +325,8 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   p.b0 = opt.b0;
   p.h0 = opt.h0;
   p.H_total = opt.H_total;
+  p.bias = opt.bias;
+  p.bias_to_raw = 1.0f / scale;
   p.lse = lse;
   p.err = error_word();
   p.wait_limit_ns = wait_limit_ns();
@@ -399,6 +444,8 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   p.b0 = opt.b0;
   p.h0 = opt.h0;
   p.H_total = opt.H_total;
+  p.bias = opt.bias;
+  p.dbias = opt.dbias;
   p.dq_acc = dq_acc;
   p.dq_part = opt.det ? dq_region : nullptr;
   p.part_stride = static_cast<size_t>(slice);
@@ -406,6 +453,12 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   p.delta = delta;
   p.err = err;
   p.wait_limit_ns = wait_limit_ns();
+  if (opt.dbias.data != nullptr && is_causal) {
+    // key tiles above the diagonal are never visited: their dbias is 0
+    e = launch_dbias_zero_causal(opt.dbias, static_cast<int>(B), static_cast<int>(H),
+                                 static_cast<int>(Sq), static_cast<int>(Sk), stream);
+    if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  }
   e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
 

@@ -129,6 +129,24 @@ __global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
   }
 }
 
+// One warp per dbias row i: zeroes keys [128 (i/128 + 1), Sk), which no key
+// tile of a causal backward writes for that row.
+__global__ void __launch_bounds__(256) dbias_zero_causal_kernel(DBias t, int B, int H, int Sq,
+                                                                int Sk) {
+  const int64_t rows = static_cast<int64_t>(B) * H * Sq;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32; row < rows;
+       row += warps) {
+    const int64_t bh = row / Sq;
+    const int i = static_cast<int>(row - bh * Sq);
+    const int b = static_cast<int>(bh / H);
+    const int h = static_cast<int>(bh - static_cast<int64_t>(b) * H);
+    uint16_t* r = t.data + b * t.sB + h * t.sH + static_cast<int64_t>(i) * t.sS;
+    for (int j = 128 * (i / 128 + 1) + lane; j < Sk; j += 32) r[j] = 0;
+  }
+}
+
 __global__ void __launch_bounds__(256) zero_fill_kernel(StridedBf16 t, int B, int H, int S, int D) {
   const int cpr = D / 8;
   const int64_t total = static_cast<int64_t>(B) * H * S * cpr;
@@ -236,7 +254,7 @@ __device__ __forceinline__ void store_row_bf16_sw128(uint32_t base, int row, con
   }
 }
 
-template <int D, bool CAUSAL, bool DROPOUT>
+template <int D, bool CAUSAL, bool DROPOUT, bool BIAS>
 __global__ void __launch_bounds__(320, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -433,6 +451,18 @@ __global__ void __launch_bounds__(320, 1)
       const int i0 = (qt_first + t) * MQ;
       const uint32_t lse_s = sb + L::kLse + st * MQ * 4;
       const uint32_t del_s = sb + L::kDelta + st * MQ * 4;
+      const bool key_ok = kj < p.Sk;
+      const uint16_t* bp = BIAS ? p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0)
+                                : nullptr;
+      if (BIAS) {
+        // this step's bias lines (a warp's 32 keys of each query row share
+        // one line): each lane starts 4 of the MQ rows towards L2
+#pragma unroll
+        for (int u = 0; u < MQ / 32; ++u) {
+          const int qi = i0 + (MQ / 32) * (r & 31) + u;
+          if (qi < p.Sq) prefetch_l2(bp + static_cast<int64_t>(qi) * p.bias.sS);
+        }
+      }
       mbar_wait(&q_full[st], (t / S) & 1, wc, kSiteBwdQFull);
       mbar_wait(s_full, t & 1, wc, kSiteBwdSFull);
       tc_fence_after();
@@ -442,10 +472,31 @@ __global__ void __launch_bounds__(320, 1)
       // visible query rows of this key: qi >= kj (causal) and the key exists
       const int first_vis = kj >= p.Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
 #pragma unroll
-      for (int c = 0; c < MQ; ++c) {
-        float e = ex2_approx(fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4)));
-        if (need_mask && c < first_vis) e = 0.f;
-        pv[c] = e;
+      for (int cc = 0; cc < MQ / 32; ++cc) {
+        uint32_t bpk[16];  // bias of query rows i0 + 32cc .. +32 at key kj, bf16 pairs
+        if (BIAS) {
+#pragma unroll
+          for (int c2 = 0; c2 < 16; ++c2) {
+            const int ia = i0 + 32 * cc + 2 * c2;
+            const uint32_t lo =
+                (key_ok && ia < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
+            const uint32_t hi = (key_ok && ia + 1 < p.Sq)
+                                    ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS)
+                                    : 0u;
+            bpk[c2] = lo | (hi << 16);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 32 * cc + i;
+          float arg = fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4));
+          if (BIAS)
+            arg = fmaf(bf16_bits_to_float((i & 1) ? (bpk[i >> 1] >> 16) : (bpk[i >> 1] & 0xffffu)),
+                       kLog2e, arg);
+          float e = ex2_approx(arg);
+          if (need_mask && c < first_vis) e = 0.f;
+          pv[c] = e;
+        }
       }
       uint32_t kb[MQ / 32];
 #pragma unroll
@@ -489,6 +540,17 @@ __global__ void __launch_bounds__(320, 1)
           float g = __uint_as_float(d[i]);
           if (DROPOUT) g = ((kb[cc] >> i) & 1u) ? g * p.drop_rescale : 0.f;
           ds[i] = pv[e] * (g - ld_shared_f32(del_s + e * 4));
+        }
+        if (BIAS && p.dbias.data != nullptr && key_ok) {
+          // dbias(i, kj) = dS(i, kj); a warp writes 64 contiguous bytes per row
+          uint16_t* dp = p.dbias.data + b * p.dbias.sB + h * p.dbias.sH + kj;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int qi = i0 + cc * 32 + i;
+            if (qi < p.Sq)
+              dp[static_cast<int64_t>(qi) * p.dbias.sS] =
+                  static_cast<uint16_t>(pack_bf16x2(ds[i], 0.f) & 0xffffu);
+          }
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -612,11 +674,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool C, bool DR>
+template <int D, bool C, bool DR, bool BI>
 cudaError_t launch_bwd_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_main_kernel<D, C, DR>;
+  auto kern = bwd_main_kernel<D, C, DR, BI>;
   const int smem = BwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<bwd_main_kernel<D, C, DR>>(smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel<D, C, DR, BI>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, 320, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
@@ -652,6 +714,14 @@ cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_dbias_zero_causal(const DBias& t, int B, int H, int Sq, int Sk,
+                                     cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(B) * H * Sq;
+  if (rows == 0 || Sk == 0) return cudaSuccess;
+  dbias_zero_causal_kernel<<<elementwise_grid(rows * 32), 256, 0, stream>>>(t, B, H, Sq, Sk);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(B) * H * S * (D / 8);
   if (items == 0) return cudaSuccess;
@@ -661,8 +731,11 @@ cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStre
 
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout, const CUtensorMap* maps,
                             const BwdParams& p, cudaStream_t stream) {
-#define SDPA_BWD_CASE(DD, CC, RR) \
-  if (D == DD && causal == CC && dropout == RR) return launch_bwd_t<DD, CC, RR>(maps, p, stream);
+  const bool bias = p.bias.data != nullptr;
+#define SDPA_BWD_CASE(DD, CC, RR)                                                    \
+  if (D == DD && causal == CC && dropout == RR)                                      \
+    return bias ? launch_bwd_t<DD, CC, RR, true>(maps, p, stream)                    \
+                : launch_bwd_t<DD, CC, RR, false>(maps, p, stream);
   SDPA_BWD_CASE(64, false, false)
   SDPA_BWD_CASE(64, false, true)
   SDPA_BWD_CASE(64, true, false)

@@ -71,7 +71,7 @@ __device__ __forceinline__ void touch32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool CAUSAL, bool DROPOUT>
+template <bool CAUSAL, bool DROPOUT, bool BIAS>
 __global__ void __launch_bounds__(448, 1)
     bwd_main_kernel_d128(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -276,6 +276,22 @@ __global__ void __launch_bounds__(448, 1)
       const int i0 = (qt_first + t) * MQ;
       const uint32_t lse_s = sb + L::kLse + st * MQ * 4;
       const uint32_t del_s = sb + L::kDelta + st * MQ * 4;
+      // bias(i0 + c, kj) of this step as bf16 pairs (c even: low half),
+      // fetched before the waits so that its latency is hidden
+      uint32_t bpk[MQ / 2];
+      if (BIAS) {
+        const bool key_ok = kj < p.Sk;
+        const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0);
+#pragma unroll
+        for (int c2 = 0; c2 < MQ / 2; ++c2) {
+          const int ia = i0 + 2 * c2;
+          const uint32_t lo =
+              (key_ok && ia < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
+          const uint32_t hi =
+              (key_ok && ia + 1 < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS) : 0u;
+          bpk[c2] = lo | (hi << 16);
+        }
+      }
       mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
       mbar_wait(&s_full[x], k & 1, wc, kSiteBwdSFull);
       tc_fence_after();
@@ -296,7 +312,11 @@ __global__ void __launch_bounds__(448, 1)
       const int first_vis = kj >= p.Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
 #pragma unroll
       for (int c = 0; c < MQ; ++c) {
-        float e = ex2_approx(fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4)));
+        float arg = fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4));
+        if (BIAS)
+          arg = fmaf(bf16_bits_to_float((c & 1) ? (bpk[c >> 1] >> 16) : (bpk[c >> 1] & 0xffffu)),
+                     kLog2e, arg);
+        float e = ex2_approx(arg);
         if (need_mask && c < first_vis) e = 0.f;
         pv[c] = e;
       }
@@ -346,6 +366,17 @@ __global__ void __launch_bounds__(448, 1)
           float g = __uint_as_float(d[i]);
           if (DROPOUT) g = ((kb[cc] >> i) & 1u) ? g * p.drop_rescale : 0.f;
           ds[i] = pv[e] * (g - ld_shared_f32(del_s + e * 4));
+        }
+        if (BIAS && p.dbias.data != nullptr && kj < p.Sk) {
+          // dbias(i, kj) = dS(i, kj); a warp writes 64 contiguous bytes per row
+          uint16_t* dp = p.dbias.data + b * p.dbias.sB + h * p.dbias.sH + kj;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int qi = i0 + cc * 32 + i;
+            if (qi < p.Sq)
+              dp[static_cast<int64_t>(qi) * p.dbias.sS] =
+                  static_cast<uint16_t>(pack_bf16x2(ds[i], 0.f) & 0xffffu);
+          }
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -453,11 +484,11 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-template <bool C, bool DR>
+template <bool C, bool DR, bool BI>
 cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_main_kernel_d128<C, DR>;
+  auto kern = bwd_main_kernel_d128<C, DR, BI>;
   const int smem = B128::kAlloc;
-  cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR>>(smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR, BI>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, B128::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
@@ -470,10 +501,16 @@ size_t bwd_d128_smem_bytes() { return B128::kAlloc; }
 
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout, const CUtensorMap* maps,
                                  const BwdParams& p, cudaStream_t stream) {
-  if (causal && dropout) return launch_t<true, true>(maps, p, stream);
-  if (causal) return launch_t<true, false>(maps, p, stream);
-  if (dropout) return launch_t<false, true>(maps, p, stream);
-  return launch_t<false, false>(maps, p, stream);
+  if (p.bias.data != nullptr) {
+    if (causal && dropout) return launch_t<true, true, true>(maps, p, stream);
+    if (causal) return launch_t<true, false, true>(maps, p, stream);
+    if (dropout) return launch_t<false, true, true>(maps, p, stream);
+    return launch_t<false, false, true>(maps, p, stream);
+  }
+  if (causal && dropout) return launch_t<true, true, false>(maps, p, stream);
+  if (causal) return launch_t<true, false, false>(maps, p, stream);
+  if (dropout) return launch_t<false, true, false>(maps, p, stream);
+  return launch_t<false, false, false>(maps, p, stream);
 }
 
 }  // namespace sdpa

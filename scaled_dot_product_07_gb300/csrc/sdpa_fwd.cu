@@ -82,7 +82,7 @@ __device__ __forceinline__ int kv_tiles_for(int r0, int Sq, int Sk, bool causal)
   return min(n, min(r0 + 127, Sq - 1) / 128 + 1);
 }
 
-template <int D, bool CAUSAL, bool DROPOUT>
+template <int D, bool CAUSAL, bool DROPOUT, bool BIAS>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -278,6 +278,27 @@ __global__ void __launch_bounds__(320, 1)
         const int qi = q0 + 128 * i + row;
         const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
         const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+        // the half row's 64 bias values, fetched before the scores are ready
+        uint4 bv[8];
+        if (BIAS) {
+          const int kb = j * 128 + 64 * half;
+          const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                               static_cast<int64_t>(min(qi, p.Sq - 1)) * p.bias.sS + kb;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (kb + 8 * c + 8 <= p.Sk) {
+              bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
+            } else {
+              // key tail: only the keys that exist are read
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (kb + 8 * c + e < p.Sk)
+                  w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
+              bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
         mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
         tc_fence_after();
         uint32_t r0[32], r1[32];
@@ -290,6 +311,19 @@ __global__ void __launch_bounds__(320, 1)
         for (int c = 0; c < 32; ++c) {
           x[c] = __uint_as_float(r0[c]);
           x[32 + c] = __uint_as_float(r1[c]);
+        }
+        if (BIAS) {
+          // the bias in raw-score units (scores are scaled at the exponential)
+          const float inv = p.bias_to_raw;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              x[8 * c + 2 * e] = fmaf(bf16_bits_to_float(w[e] & 0xffffu), inv, x[8 * c + 2 * e]);
+              x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
+            }
+          }
         }
         const int k0 = j * 128 + 64 * half;  // first key of this half
         if ((k0 + 64 > p.Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
@@ -419,11 +453,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool C, bool DR>
+template <int D, bool C, bool DR, bool BI>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<D, C, DR>;
+  auto kern = fwd_kernel<D, C, DR, BI>;
   const int smem = FwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR>>(smem);
+  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, BI>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
@@ -438,8 +472,11 @@ size_t fwd_smem_bytes(int D) {
 
 cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps,
                        const FwdParams& p, cudaStream_t stream) {
-#define SDPA_FWD_CASE(DD, CC, RR) \
-  if (D == DD && causal == CC && dropout == RR) return launch_fwd_t<DD, CC, RR>(maps, p, stream);
+  const bool bias = p.bias.data != nullptr;
+#define SDPA_FWD_CASE(DD, CC, RR)                                                    \
+  if (D == DD && causal == CC && dropout == RR)                                      \
+    return bias ? launch_fwd_t<DD, CC, RR, true>(maps, p, stream)                    \
+                : launch_fwd_t<DD, CC, RR, false>(maps, p, stream);
   SDPA_FWD_CASE(64, false, false)
   SDPA_FWD_CASE(64, false, true)
   SDPA_FWD_CASE(64, true, false)

@@ -112,3 +112,39 @@ def empty_like_layout(shape, layout, dtype, device):
     if layout == "BSHE":
         return torch.empty((B, S, H, D), dtype=dtype, device=device).permute(0, 2, 1, 3)
     raise ValueError(f"unknown layout {layout}")
+
+
+def draw_bias(shape, seed, kind="random"):
+    """Seeded bfloat16 additive-bias input of logical shape [Bb, Hb, Sq, Sk]
+    (CPU, contiguous).
+
+    ``random``: float32 ``randn`` from a CPU generator seeded with ``seed``,
+    times 1.5. ``relpos``: a relative-position pattern, -slope_h * |i - j|
+    with slope_h = 2^(-(h + 1) / Hb) (distance penalties of different
+    strength per head), plus the same random draw times 0.1. Both are
+    rounded to bfloat16; only inputs are made here.
+    """
+    Bb, Hb, Sq, Sk = shape
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    noise = torch.randn(shape, generator=g, dtype=torch.float32)
+    if kind == "random":
+        x = noise * 1.5
+    elif kind == "relpos":
+        dist = (torch.arange(Sq)[:, None] - torch.arange(Sk)[None, :]).abs().float()
+        slope = torch.pow(2.0, -(torch.arange(Hb, dtype=torch.float32) + 1.0) / Hb)
+        x = -slope[None, :, None, None] * dist[None, None] + 0.1 * noise
+    else:
+        raise ValueError(f"unknown bias kind {kind}")
+    return x.to(torch.bfloat16)
+
+
+def padded_rows(x, multiple=8):
+    """The same logical [.., Sk] values in a buffer whose key rows are padded
+    to a multiple of ``multiple`` elements (a view with a larger row stride),
+    as the bias loads of the kernels require 16-byte aligned rows."""
+    Sk = x.shape[-1]
+    pad = (Sk + multiple - 1) // multiple * multiple
+    buf = torch.zeros(x.shape[:-1] + (pad,), dtype=x.dtype, device=x.device)
+    buf[..., :Sk] = x
+    return buf[..., :Sk]

@@ -222,3 +222,33 @@ def test_option_errors_are_reported_before_any_launch(lib):
     assert bwd(options(head_offset=2, total_heads=5), plain) == 1
     assert lib.sdpa_dropout_mask_debug_ex(B, H, S, S, 0.1, 0, 0, r(options(head_offset=9)),
                                           ctypes.c_void_p(FAKE), None) == 1
+
+
+def test_bias_argument_errors(lib):
+    B, H, Sq, Sk, D = 2, 4, 100, 130, 64
+    q, kk = desc(B, H, Sq, D), desc(B, H, Sk, D)
+    r = ctypes.byref
+    keep = []  # descriptors must outlive the calls that point at them
+
+    def bias(Bb=B, Hb=H, S1=Sq, S2=Sk, row=136, data=FAKE, key_stride=1):
+        d = desc(Bb, Hb, S1, S2, data=data, stride=(Hb * S1 * row, S1 * row, row, key_stride))
+        keep.append(d)
+        return ctypes.addressof(d)
+
+    def fwd(o):
+        return lib.sdpa_fwd_ex(r(q), r(kk), r(kk), 0.0, 1, 0.125, 1, 0, r(q), ctypes.c_void_p(FAKE),
+                               r(o), None)
+
+    assert fwd(options(attn_bias=bias(Bb=3))) == 1           # batch 3 vs 2
+    assert fwd(options(attn_bias=bias(S2=Sk + 1))) == 1      # key length
+    assert fwd(options(attn_bias=bias(row=130))) == 3        # rows not 16-byte aligned
+    assert fwd(options(attn_bias=bias(data=FAKE + 2))) == 3  # base not aligned
+    assert fwd(options(attn_bias=bias(key_stride=2))) == 2   # keys not contiguous
+
+    def bwd(o):
+        return lib.sdpa_bwd_ex(r(q), r(q), r(kk), r(kk), r(q), ctypes.c_void_p(FAKE), 0.0, 1, 0, 0,
+                               0.125, r(q), r(kk), r(kk), ctypes.c_void_p(FAKE), 1 << 40, r(o), None)
+
+    # a gradient needs the bias, and must have the full [B, H, Sq, Sk] shape
+    assert bwd(options(dbias=bias())) == 1
+    assert bwd(options(attn_bias=bias(Bb=1, Hb=1), dbias=bias(Bb=1))) == 1
