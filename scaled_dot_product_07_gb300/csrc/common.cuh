@@ -54,6 +54,7 @@ struct FwdParams {
   int b0, h0, H_total;      // counter position of this launch in the whole problem
   AttnBias bias;
   float bias_to_raw;        // 1 / scale
+  int h_major;              // CTA order by head, then batch (a batch-shared bias stays in L2)
   float* lse;             // [B, H, Sq] fp32
   uint32_t* err;          // device error word
   uint64_t wait_limit_ns;
@@ -71,6 +72,7 @@ struct BwdParams {
   int b0, h0, H_total;
   AttnBias bias;
   DBias dbias;
+  int h_major;
   float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
   float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
   size_t part_stride;     // one plain-stored partial per key tile (floats per slice)

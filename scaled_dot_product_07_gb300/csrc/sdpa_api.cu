@@ -327,6 +327,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   p.H_total = opt.H_total;
   p.bias = opt.bias;
   p.bias_to_raw = 1.0f / scale;
+  p.h_major = (opt.bias.data != nullptr && opt.bias.sB == 0 && B > 1) ? 1 : 0;
   p.lse = lse;
   p.err = error_word();
   p.wait_limit_ns = wait_limit_ns();
@@ -446,6 +447,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   p.H_total = opt.H_total;
   p.bias = opt.bias;
   p.dbias = opt.dbias;
+  p.h_major = (opt.bias.data != nullptr && opt.bias.sB == 0 && B > 1) ? 1 : 0;
   p.dq_acc = dq_acc;
   p.dq_part = opt.det ? dq_region : nullptr;
   p.part_stride = static_cast<size_t>(slice);

@@ -289,10 +289,12 @@ __global__ void __launch_bounds__(320, 1)
   // head-major order: the CTAs of one head run together, so the head's Q and
   // dO tiles (which every one of them streams) stay in L2; within a head the
   // low key tiles (the most causal work) go first
-  const int bh = blockIdx.x / p.n_kv_tiles;
-  const int kv_tile = blockIdx.x - bh * p.n_kv_tiles;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
+  const int slot = blockIdx.x / p.n_kv_tiles;
+  const int kv_tile = blockIdx.x - slot * p.n_kv_tiles;
+  // batch-major, or head-major when the bias is shared by the batch
+  const int b = p.h_major ? slot % p.B : slot / p.H;
+  const int h = p.h_major ? slot / p.B : slot - b * p.H;
+  const int bh = b * p.H + h;
   const int k0 = kv_tile * 128;
   const int n_qt = (p.Sq + MQ - 1) / MQ;
   const int qt_first = CAUSAL ? min(k0 / MQ, n_qt) : 0;
@@ -454,15 +456,6 @@ __global__ void __launch_bounds__(320, 1)
       const bool key_ok = kj < p.Sk;
       const uint16_t* bp = BIAS ? p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0)
                                 : nullptr;
-      if (BIAS) {
-        // this step's bias lines (a warp's 32 keys of each query row share
-        // one line): each lane starts 4 of the MQ rows towards L2
-#pragma unroll
-        for (int u = 0; u < MQ / 32; ++u) {
-          const int qi = i0 + (MQ / 32) * (r & 31) + u;
-          if (qi < p.Sq) prefetch_l2(bp + static_cast<int64_t>(qi) * p.bias.sS);
-        }
-      }
       mbar_wait(&q_full[st], (t / S) & 1, wc, kSiteBwdQFull);
       mbar_wait(s_full, t & 1, wc, kSiteBwdSFull);
       tc_fence_after();

@@ -107,10 +107,12 @@ __global__ void __launch_bounds__(448, 1)
   const int lane = threadIdx.x & 31;
   // head-major order (a head's Q and dO stay in L2 while its key tiles run);
   // low key tiles, which see the most causal query rows, first
-  const int bh = blockIdx.x / p.n_kv_tiles;
-  const int kv_tile = blockIdx.x - bh * p.n_kv_tiles;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
+  const int slot = blockIdx.x / p.n_kv_tiles;
+  const int kv_tile = blockIdx.x - slot * p.n_kv_tiles;
+  // batch-major, or head-major when the bias is shared by the batch
+  const int b = p.h_major ? slot % p.B : slot / p.H;
+  const int h = p.h_major ? slot / p.B : slot - b * p.H;
+  const int bh = b * p.H + h;
   const int k0 = kv_tile * 128;
   const int n_qt = (p.Sq + MQ - 1) / MQ;
   const int qt_first = CAUSAL ? min(k0 / MQ, n_qt) : 0;

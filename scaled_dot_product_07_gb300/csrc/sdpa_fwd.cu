@@ -112,11 +112,14 @@ __global__ void __launch_bounds__(320, 1)
   // head-major order (a head's K/V stays in L2 while its tiles run);
   // within a head the longest causal tiles go first
   const int n_pairs = p.n_q_tiles;  // tile pairs per head
-  const int bh = blockIdx.x / n_pairs;
-  int pair = blockIdx.x - bh * n_pairs;
+  const int slot = blockIdx.x / n_pairs;
+  int pair = blockIdx.x - slot * n_pairs;
   if (CAUSAL) pair = n_pairs - 1 - pair;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
+  // (b, h) of this CTA: batch-major, or head-major when a bias shared by the
+  // batch makes the batches of one head read the same bias tiles
+  const int b = p.h_major ? slot % p.B : slot / p.H;
+  const int h = p.h_major ? slot / p.B : slot - b * p.H;
+  const int bh = b * p.H + h;
   const int q0 = pair * 256;
   const int n_t[2] = {kv_tiles_for(q0, p.Sq, p.Sk, CAUSAL),
                       kv_tiles_for(q0 + 128, p.Sq, p.Sk, CAUSAL)};
@@ -281,6 +284,14 @@ __global__ void __launch_bounds__(320, 1)
         // the half row's 64 bias values, fetched before the scores are ready
         uint4 bv[8];
         if (BIAS) {
+          // start the next key tile's bias line towards L2
+          const int kn = (j + 1) * 128 + 64 * half;
+          if (j + 1 < n_t[i] && kn < p.Sk) {
+            const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                                 static_cast<int64_t>(min(qi, p.Sq - 1)) * p.bias.sS + kn;
+            prefetch_l2(np);
+            prefetch_l2(np + min(56, p.Sk - 1 - kn));
+          }
           const int kb = j * 128 + 64 * half;
           const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
                                static_cast<int64_t>(min(qi, p.Sq - 1)) * p.bias.sS + kb;
