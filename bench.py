@@ -19,14 +19,15 @@ roofline    the backward (dominant) and forward kernels against the measured
 extended    the options entry points on the same workload: the step recorded
             once as a CUDA graph (rng state read from device memory) and
             replayed, and the deterministic (fixed-order dQ) backward; the
-            same shape at head dim 96; and with an additive relative-position
-            bias (and its gradient).
+            same shape at head dim 96; with an additive relative-position
+            bias (and its gradient); and a packed batch of mixed lengths.
 cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
             the same workload (whole heads), on this host's cores.
 """
 
 import argparse
 import hashlib
+import itertools
 import json
 import os
 import statistics
@@ -406,6 +407,32 @@ def bench_ours(args, w):
             "note": "bf16 relative-position bias [1,H,Sq,Sk] shared by the batch; the backward "
                     "also writes dbias [B,H,Sq,Sk] bf16"}
         del bias, dbias
+        # a packed batch of causal sequences of mixed lengths (the decoder's
+        # heads and head dim), through the variable-length entry points
+        lens = [4096, 2048, 3072, 1024, 4096, 512, 3584, 2560]
+        H, D = w.H, w.D
+        tot = sum(lens)
+        gv = torch.Generator(device="cpu")
+        gv.manual_seed(w.input_seed + 29)
+        pq, pk, pv, pdo = (torch.randn((tot, H, D), generator=gv).to(torch.bfloat16).to(dev)
+                           for _ in range(4))
+        cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=dev)
+        pout = torch.empty_like(pq)
+        plse = torch.empty((H, tot), dtype=torch.float32, device=dev)
+        pdq, pdk, pdv = torch.empty_like(pq), torch.empty_like(pk), torch.empty_like(pv)
+        pws = torch.empty(sdpa.sdpa_bwd_varlen_workspace_size(cu, cu, max(lens), max(lens), H, D),
+                          dtype=torch.uint8, device=dev)
+        fwd_v = timed(lambda: sdpa.sdpa_fwd_varlen(pq, pk, pv, cu, cu, max(lens), max(lens), 0.0,
+                                                   True, None, 0, 0, out=pout, lse=plse), 5)
+        bwd_v = timed(lambda: sdpa.sdpa_bwd_varlen(pdo, pq, pk, pv, pout, plse, cu, cu, max(lens),
+                                                   max(lens), 0.0, True, 0, 0, dq=pdq, dk=pdk,
+                                                   dv=pdv, workspace=pws), 5)
+        vpairs = sum(n * (n + 1) // 2 for n in lens) * H
+        extras["varlen"] = {
+            "fwd_ms": fwd_v, "fwd_tflops": 4 * D * vpairs / (fwd_v * 1e-3) / 1e12,
+            "bwd_ms": bwd_v, "bwd_tflops": 10 * D * vpairs / (bwd_v * 1e-3) / 1e12,
+            "note": f"packed causal batch, lengths {lens}, H{H} D{D}"}
+        del pq, pk, pv, pdo, pout, plse, pdq, pdk, pdv, pws
         if sdpa.sdpa_check_device() != 0:
             raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
 

@@ -245,6 +245,55 @@ sdpa_status sdpa_dropout_mask_debug_ex(int64_t B, int64_t H, int64_t Sq, int64_t
                                        sdpa_stream_t stream);
 
 /*
+ * Packed variable-length batches. The fused kernels' forward also reports
+ * the maximum query and key lengths (max_q / max_k: "Note to self: Next few
+ * PRs" of NVIDIA/Fuser issue 2278, "SdpaOpFwd / SdpaOpBwd nodes"), the
+ * sizes of a batch of sequences of different lengths stored back to back.
+ * Sequence b of `batch` has query rows [cu_seqlens_q[b], cu_seqlens_q[b+1])
+ * of q, out, dout and dq, and key rows [cu_seqlens_k[b], cu_seqlens_k[b+1])
+ * of k, v, dk and dv. The tensors are logical [1, H, total, D] (e.g. a
+ * packed [total, H, D] buffer viewed with strides (_, D, H*D, 1)), lse is
+ * float32 [H, total_q] contiguous. Each sequence is computed as the top-left
+ * [len_q, len_k] block of a [max_seqlen_q, max_seqlen_k] problem: causal
+ * masking is top-left within the sequence, and the dropout counter uses the
+ * padded problem's index, ((b*H + h)*max_seqlen_q + i)*max_seqlen_k + j.
+ *   cu_seqlens_q, cu_seqlens_k: device int32 arrays of batch + 1 offsets,
+ *     starting at 0, nondecreasing, ending at the tensors' totals. They are
+ *     read on the device only, so the host cannot check them; lengths above
+ *     the maxima are not allowed. A sequence with queries and no keys gets
+ *     out = 0 and lse = -inf.
+ *   max_seqlen_q, max_seqlen_k: bounds (>= 1) of the sequences' lengths;
+ *     they size the launch grids and the backward workspace.
+ * sdpa_options apply as in the *_ex calls, except attn_bias / dbias
+ * (SDPA_ERR_UNSUPPORTED with a packed batch).
+ */
+typedef struct {
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int64_t batch;
+  int64_t max_seqlen_q;
+  int64_t max_seqlen_k;
+} sdpa_varlen;
+
+sdpa_status sdpa_fwd_varlen(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                            const sdpa_varlen* seqs, double dropout_p, int is_causal, float scale,
+                            uint64_t seed, uint64_t offset, sdpa_tensor* out, float* lse,
+                            const sdpa_options* options, sdpa_stream_t stream);
+
+/* Workspace bytes of sdpa_bwd_varlen: as sdpa_bwd_workspace_size_ex with B =
+ * batch, Sq = max_seqlen_q, Sk = max_seqlen_k. */
+size_t sdpa_bwd_varlen_workspace_size(const sdpa_varlen* seqs, int64_t H, int64_t D,
+                                      const sdpa_options* options);
+
+sdpa_status sdpa_bwd_varlen(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                            const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                            const sdpa_varlen* seqs, double dropout_p, int is_causal,
+                            uint64_t seed, uint64_t offset, float scale, sdpa_tensor* dq,
+                            sdpa_tensor* dk, sdpa_tensor* dv, void* workspace,
+                            size_t workspace_bytes, const sdpa_options* options,
+                            sdpa_stream_t stream);
+
+/*
  * sdpa_check_device — synchronises `stream`, then reports whether any kernel
  * of this library on the current device gave up on a bounded wait since the
  * last check (SDPA_ERR_DEVICE_TIMEOUT; the word is cleared) or the stream

@@ -27,6 +27,7 @@ __all__ = [
     "sdpa_selftest_wait_timeout", "sdpa_status_string", "SDPAFunction", "EXPORTED_SYMBOLS",
     "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "sdpa_fwd_ex", "sdpa_bwd_ex",
     "sdpa_bwd_workspace_size_ex", "sdpa_dropout_mask_debug_ex", "SdpaOptions",
+    "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_bwd_varlen_workspace_size", "SdpaVarlen",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "sdpa_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_dropout_mask_debug",
     "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string", "sdpa_bwd_noalloc",
     "sdpa_fwd_ex", "sdpa_bwd_workspace_size_ex", "sdpa_bwd_ex", "sdpa_dropout_mask_debug_ex",
+    "sdpa_fwd_varlen", "sdpa_bwd_varlen_workspace_size", "sdpa_bwd_varlen",
 )
 
 # SDPA_BWD_NOALLOC_SCRATCH_BYTES of include/sdpa.h
@@ -60,6 +62,13 @@ class SdpaError(RuntimeError):
 class SdpaTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("size", ctypes.c_int64 * 4),
                 ("stride", ctypes.c_int64 * 4)]
+
+
+class SdpaVarlen(ctypes.Structure):
+    """sdpa_varlen of include/sdpa.h."""
+    _fields_ = [("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+                ("batch", ctypes.c_int64), ("max_seqlen_q", ctypes.c_int64),
+                ("max_seqlen_k", ctypes.c_int64)]
 
 
 class SdpaOptions(ctypes.Structure):
@@ -108,6 +117,13 @@ def load_library(path=None):
     lib.sdpa_bwd_ex.restype = ctypes.c_int
     lib.sdpa_dropout_mask_debug_ex.argtypes = [i64, i64, i64, i64, dbl, u64, u64, vp, vp, vp]
     lib.sdpa_dropout_mask_debug_ex.restype = ctypes.c_int
+    lib.sdpa_fwd_varlen.argtypes = [P, P, P, vp, dbl, ctypes.c_int, flt, u64, u64, P, vp, vp, vp]
+    lib.sdpa_fwd_varlen.restype = ctypes.c_int
+    lib.sdpa_bwd_varlen_workspace_size.argtypes = [vp, i64, i64, vp]
+    lib.sdpa_bwd_varlen_workspace_size.restype = ctypes.c_size_t
+    lib.sdpa_bwd_varlen.argtypes = [P, P, P, P, P, vp, vp, dbl, ctypes.c_int, u64, u64, flt, P, P,
+                                    P, vp, ctypes.c_size_t, vp, vp]
+    lib.sdpa_bwd_varlen.restype = ctypes.c_int
     lib.sdpa_check_device.argtypes = [vp]
     lib.sdpa_check_device.restype = ctypes.c_int
     lib.sdpa_selftest_wait_timeout.argtypes = [u64, vp]
@@ -377,6 +393,100 @@ def sdpa_dropout_mask_debug_ex(B, H, Sq, Sk, dropout_p, seed=0, offset=0, rng_st
                                         _stream(mask.device))
     _check(st, "sdpa_dropout_mask_debug_ex")
     return mask
+
+
+def _packed(t, name):
+    """Descriptor of a packed [total, H, D] tensor as the logical [1, H, total, D]."""
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be a packed [total, H, D] tensor")
+    return _desc(t.permute(1, 0, 2).unsqueeze(0))
+
+
+def _varlen(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k):
+    import torch
+    for c, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        if not c.is_cuda or c.dtype != torch.int32 or c.dim() != 1:
+            raise ValueError(f"{n} must be a 1-D int32 CUDA tensor of batch + 1 offsets")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold batch + 1 offsets")
+    vl = SdpaVarlen()
+    vl.cu_seqlens_q = cu_seqlens_q.data_ptr()
+    vl.cu_seqlens_k = cu_seqlens_k.data_ptr()
+    vl.batch = cu_seqlens_q.numel() - 1
+    vl.max_seqlen_q = int(max_seqlen_q)
+    vl.max_seqlen_k = int(max_seqlen_k)
+    return vl
+
+
+def sdpa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    dropout_p=0.0, is_causal=False, scale=None, seed=None, offset=None,
+                    rng_state=None, batch_offset=0, head_offset=0, total_heads=0, out=None,
+                    lse=None):
+    """Forward of a packed batch: q [total_q, H, D], k, v [total_k, H, D];
+    sequence b is rows cu_seqlens_q[b]:cu_seqlens_q[b+1] (queries) and
+    cu_seqlens_k[b]:cu_seqlens_k[b+1] (keys). Returns (out [total_q, H, D],
+    lse [H, total_q], seed, offset)."""
+    import torch
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    Tq, H, D = q.shape
+    if seed is None:
+        seed = int(torch.randint(0, 2**62, (1,)).item()) if dropout_p > 0 else 0
+    if offset is None:
+        offset = 0
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=q.device) if lse is None else lse
+    vl = _varlen(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads)
+    dq_, dk_, dv_, do_ = _packed(q, "q"), _packed(k, "k"), _packed(v, "v"), _packed(out, "out")
+    st = lib.sdpa_fwd_varlen(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_),
+                             ctypes.byref(vl), float(dropout_p), int(bool(is_causal)),
+                             _default_scale(D, scale), int(seed), int(offset), ctypes.byref(do_),
+                             ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                             ctypes.byref(opt), _stream(q.device))
+    _check(st, "sdpa_fwd_varlen")
+    return out, lse, seed, offset
+
+
+def sdpa_bwd_varlen_workspace_size(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, H, D,
+                                   deterministic=False):
+    vl = _varlen(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    opt = _options(deterministic=deterministic)
+    return int(load_library().sdpa_bwd_varlen_workspace_size(ctypes.byref(vl), H, D,
+                                                             ctypes.byref(opt)))
+
+
+def sdpa_bwd_varlen(dout, q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                    max_seqlen_k, dropout_p=0.0, is_causal=False, seed=0, offset=0, scale=None,
+                    rng_state=None, batch_offset=0, head_offset=0, total_heads=0,
+                    deterministic=False, dq=None, dk=None, dv=None, workspace=None):
+    """Backward of a packed batch (see :func:`sdpa_fwd_varlen`). Returns
+    (dq, dk, dv) in the packed layouts of q, k, v."""
+    import torch
+    lib = load_library()
+    for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _check_tensor(t, n)
+    Tq, H, D = q.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    vl = _varlen(cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic)
+    need = int(lib.sdpa_bwd_varlen_workspace_size(ctypes.byref(vl), H, D, ctypes.byref(opt)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    descs = [_packed(t, n) for t, n in ((dout, "dout"), (q, "q"), (k, "k"), (v, "v"), (out, "out"),
+                                        (dq, "dq"), (dk, "dk"), (dv, "dv"))]
+    refs = [ctypes.byref(d) for d in descs]
+    st = lib.sdpa_bwd_varlen(refs[0], refs[1], refs[2], refs[3], refs[4],
+                             ctypes.c_void_p(lse.data_ptr() if lse.numel() else None),
+                             ctypes.byref(vl), float(dropout_p), int(bool(is_causal)), int(seed),
+                             int(offset), _default_scale(D, scale), refs[5], refs[6], refs[7],
+                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+                             ctypes.byref(opt), _stream(q.device))
+    _check(st, "sdpa_bwd_varlen")
+    return dq, dk, dv
 
 
 def sdpa_check_device(device="cuda"):

@@ -26,6 +26,12 @@ enum WaitSite : uint32_t {
   kSiteSelftest = 0x301,
 };
 
+// Strided bf16 [B,H,S,D] view used by the elementwise kernels.
+struct StridedBf16 {
+  void* data;
+  int64_t sB, sH, sS;  // element strides (D is contiguous)
+};
+
 // Additive attention bias: bf16 [B or 1, H or 1, Sq, Sk], keys contiguous;
 // a shared (size-1) batch or head dim has stride 0.
 struct AttnBias {
@@ -55,6 +61,14 @@ struct FwdParams {
   AttnBias bias;
   float bias_to_raw;        // 1 / scale
   int h_major;              // CTA order by head, then batch (a batch-shared bias stays in L2)
+  // packed variable-length batches (null: one [Sq, Sk] problem per (b, h)):
+  // sequence b is query rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1])
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int Sq_ctr, Sk_ctr;       // dims of the dropout counter (Sq, Sk; or the max lengths)
+  int total_q;              // packed query rows (lse is [H, total_q] when packed)
+  int D_io;                 // the caller's head dim (columns of out)
+  StridedBf16 out_io;       // out, for the direct stores of a sequence's last tile
   float* lse;             // [B, H, Sq] fp32
   uint32_t* err;          // device error word
   uint64_t wait_limit_ns;
@@ -73,6 +87,12 @@ struct BwdParams {
   AttnBias bias;
   DBias dbias;
   int h_major;
+  // packed variable-length batches (null: one [Sq, Sk] problem per (b, h))
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int Sq_ctr, Sk_ctr;       // dims of the dropout counter
+  int D_io;                 // the caller's head dim (columns of dk, dv)
+  StridedBf16 dk_io, dv_io; // for the direct stores of a sequence's last key tile
   float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
   float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
   size_t part_stride;     // one plain-stored partial per key tile (floats per slice)
@@ -82,17 +102,14 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
-// Strided bf16 [B,H,S,D] view used by the elementwise kernels.
-struct StridedBf16 {
-  void* data;
-  int64_t sB, sH, sS;  // element strides (D is contiguous)
-};
 
 // D is the kernels' head dim (64 or 128: the width of the fp32 dQ rows);
 // D_io the caller's head dim (a multiple of 8, at most D), the width of the
 // rows read from out / dout and written to dq.
 struct PreParams {
   int B, H, Sq, Sq_pad, D, D_io;
+  const int32_t* cu_q;    // packed batch: sequence b's rows (Sq is then the maximum length)
+  int total_q;
   StridedBf16 out, dout;
   const float* lse;       // [B,H,Sq]
   float* lse2;
@@ -102,6 +119,7 @@ struct PreParams {
 
 struct ConvParams {
   int B, H, Sq, Sq_pad, D, D_io;
+  const int32_t* cu_q;
   float scale;
   const float* dq_acc;
   StridedBf16 dq;
@@ -111,6 +129,8 @@ struct ConvParams {
 // key-tile order, of the stored partials.
 struct SumParams {
   int B, H, Sq, Sq_pad, D, D_io;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
   int n_kv_tiles;
   int causal;
   float scale;

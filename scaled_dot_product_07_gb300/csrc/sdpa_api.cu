@@ -279,34 +279,32 @@ sdpa_status finish(cudaError_t e, cudaStream_t stream) {
   return SDPA_OK;
 }
 
-}  // namespace
-}  // namespace sdpa
+// A packed batch: B >= 1 sequences whose offsets are device arrays; the
+// tensors are logical [1, H, total, D]. The offsets themselves are not read
+// here (they live in device memory): they must start at 0, not decrease,
+// end at the tensors' totals and give lengths of at most the maxima.
+sdpa_status check_varlen(const sdpa_varlen* seqs, const sdpa_tensor* q, const sdpa_tensor* k) {
+  if (!seqs || !seqs->cu_seqlens_q || !seqs->cu_seqlens_k) return SDPA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seqs->cu_seqlens_q) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seqs->cu_seqlens_k) & 3u))
+    return SDPA_ERR_ALIGNMENT;
+  if (seqs->batch < 1 || seqs->max_seqlen_q < 1 || seqs->max_seqlen_k < 1) return SDPA_ERR_INVALID_ARG;
+  if (seqs->batch > 0x7fffffff || seqs->max_seqlen_q > 0x7fffffff || seqs->max_seqlen_k > 0x7fffffff)
+    return SDPA_ERR_INVALID_ARG;
+  if (q->size[0] != 1 || k->size[0] != 1) return SDPA_ERR_INVALID_ARG;
+  if (q->size[2] > 0x7fffffff || k->size[2] > 0x7fffffff) return SDPA_ERR_INVALID_ARG;
+  return SDPA_OK;
+}
 
-using namespace sdpa;
-
-extern "C" {
-
-sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
-                        double dropout_p, int is_causal, float scale, uint64_t seed,
-                        uint64_t offset, sdpa_tensor* out, float* lse,
-                        const sdpa_options* options, sdpa_stream_t stream_) {
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  sdpa_status s = check_dims(q, k, v);
-  if (s != SDPA_OK) return s;
-  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
-  const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
-  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+// Shared tail of the forward entry points: tensor maps, parameters, launch.
+// B, Sq, Sk are the problem's (or, packed, the batch count and the maximum
+// lengths); cu_q / cu_k are null unless the batch is packed.
+sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                       sdpa_tensor* out, float* lse, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
+                       int64_t D, double dropout_p, int is_causal, float scale, uint64_t seed,
+                       uint64_t offset, const Opts& opt, const int32_t* cu_q, const int32_t* cu_k,
+                       int64_t total_q, cudaStream_t stream) {
   const int64_t Dk = kernel_head_dim(D);
-  if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
-  if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
-  if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
-  if ((s = check_tensor(out, B, H, Sq, D)) != SDPA_OK) return s;
-  if (B * H * Sq == 0) return SDPA_OK;
-  if (Sk == 0) return SDPA_ERR_INVALID_ARG;  // softmax over no keys
-  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
-  Opts opt;
-  if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
-
   CUtensorMap maps[4];
   if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
       !make_map(&maps[3], out, 128))
@@ -328,12 +326,200 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   p.bias = opt.bias;
   p.bias_to_raw = 1.0f / scale;
   p.h_major = (opt.bias.data != nullptr && opt.bias.sB == 0 && B > 1) ? 1 : 0;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.Sq_ctr = static_cast<int>(Sq);
+  p.Sk_ctr = static_cast<int>(Sk);
+  p.total_q = static_cast<int>(total_q);
+  p.D_io = static_cast<int>(D);
+  p.out_io = strided(out);
   p.lse = lse;
   p.err = error_word();
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return SDPA_ERR_CUDA;
   const bool dropout = dropout_p > 0.0;
   return finish(launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream), stream);
+}
+
+// Shared tail of the backward entry points: workspace, tensor maps, the
+// preprocess, main and dQ kernels. B, Sq, Sk are the problem's (or, packed,
+// the batch count and the maximum lengths); cu_q / cu_k are null unless the
+// batch is packed.
+sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                       const sdpa_tensor* v, const sdpa_tensor* out, const float* lse, int64_t B,
+                       int64_t H, int64_t Sq, int64_t Sk, int64_t D, double dropout_p,
+                       int is_causal, uint64_t seed, uint64_t offset, float scale, sdpa_tensor* dq,
+                       sdpa_tensor* dk, sdpa_tensor* dv, void* workspace, size_t workspace_bytes,
+                       const sdpa_options* options, const Opts& opt, const int32_t* cu_q,
+                       const int32_t* cu_k, int64_t total_q, cudaStream_t stream) {
+  const int64_t Dk = kernel_head_dim(D);
+  const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SDPA_ERR_WORKSPACE;
+
+  // workspace: [dQ accumulator | per-key-tile dQ partials (deterministic)], lse2, delta
+  const int64_t Sq_pad = round_up(Sq, 128);
+  const int64_t n_kv = (Sk + 127) / 128;
+  const int64_t slice = B * H * Sq_pad * Dk;
+  float* dq_region = static_cast<float*>(workspace);
+  float* lse2 = dq_region + slice * (opt.det ? n_kv : 1);
+  float* delta = lse2 + B * H * Sq_pad;
+  float* dq_acc = opt.det ? nullptr : dq_region;
+
+  const uint32_t mq = static_cast<uint32_t>(8192 / Dk);
+  CUtensorMap maps[6];
+  if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
+      !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
+    return SDPA_ERR_CUDA;
+
+  uint32_t* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+
+  PreParams pp;
+  pp.B = static_cast<int>(B);
+  pp.H = static_cast<int>(H);
+  pp.Sq = static_cast<int>(Sq);
+  pp.Sq_pad = static_cast<int>(Sq_pad);
+  pp.D = static_cast<int>(Dk);
+  pp.D_io = static_cast<int>(D);
+  pp.out = strided(out);
+  pp.dout = strided(dout);
+  pp.lse = lse;
+  pp.lse2 = lse2;
+  pp.delta = delta;
+  pp.dq_acc = dq_acc;
+  pp.cu_q = cu_q;
+  pp.total_q = static_cast<int>(total_q);
+  cudaError_t e = launch_bwd_preprocess(pp, stream);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+
+  BwdParams p;
+  p.B = pp.B;
+  p.H = pp.H;
+  p.Sq = pp.Sq;
+  p.Sk = static_cast<int>(Sk);
+  p.Sq_pad = pp.Sq_pad;
+  p.n_kv_tiles = static_cast<int>((Sk + 127) / 128);
+  p.scale_log2 = scale * kLog2e;
+  p.scale = scale;
+  p.drop_threshold = drop_threshold(dropout_p);
+  p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
+  p.pk = philox_key(seed, offset);
+  p.rng_dev = opt.rng;
+  p.b0 = opt.b0;
+  p.h0 = opt.h0;
+  p.H_total = opt.H_total;
+  p.bias = opt.bias;
+  p.dbias = opt.dbias;
+  p.h_major = (opt.bias.data != nullptr && opt.bias.sB == 0 && B > 1) ? 1 : 0;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.Sq_ctr = static_cast<int>(Sq);
+  p.Sk_ctr = static_cast<int>(Sk);
+  p.D_io = static_cast<int>(D);
+  p.dk_io = strided(dk);
+  p.dv_io = strided(dv);
+  p.dq_acc = dq_acc;
+  p.dq_part = opt.det ? dq_region : nullptr;
+  p.part_stride = static_cast<size_t>(slice);
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.err = err;
+  p.wait_limit_ns = wait_limit_ns();
+  if (opt.dbias.data != nullptr && is_causal) {
+    // key tiles above the diagonal are never visited: their dbias is 0
+    e = launch_dbias_zero_causal(opt.dbias, static_cast<int>(B), static_cast<int>(H),
+                                 static_cast<int>(Sq), static_cast<int>(Sk), stream);
+    if (e != cudaSuccess) return SDPA_ERR_CUDA;
+  }
+  e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
+  if (e != cudaSuccess) return SDPA_ERR_CUDA;
+
+  if (opt.det) {
+    SumParams sp;
+    sp.B = pp.B;
+    sp.H = pp.H;
+    sp.Sq = pp.Sq;
+    sp.Sq_pad = pp.Sq_pad;
+    sp.D = pp.D;
+    sp.D_io = pp.D_io;
+    sp.n_kv_tiles = p.n_kv_tiles;
+    sp.causal = is_causal != 0;
+    sp.scale = scale;
+    sp.dq_part = dq_region;
+    sp.cu_q = cu_q;
+    sp.cu_k = cu_k;
+    sp.part_stride = static_cast<size_t>(slice);
+    sp.dq = strided(dq);
+    return finish(launch_bwd_dq_sum(sp, stream), stream);
+  }
+  ConvParams cp;
+  cp.B = pp.B;
+  cp.H = pp.H;
+  cp.Sq = pp.Sq;
+  cp.Sq_pad = pp.Sq_pad;
+  cp.D = pp.D;
+  cp.D_io = pp.D_io;
+  cp.scale = scale;
+  cp.dq_acc = dq_acc;
+  cp.cu_q = cu_q;
+  cp.dq = strided(dq);
+  return finish(launch_bwd_dq_convert(cp, stream), stream);
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                        double dropout_p, int is_causal, float scale, uint64_t seed,
+                        uint64_t offset, sdpa_tensor* out, float* lse,
+                        const sdpa_options* options, sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  sdpa_status s = check_dims(q, k, v);
+  if (s != SDPA_OK) return s;
+  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
+  const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(out, B, H, Sq, D)) != SDPA_OK) return s;
+  if (B * H * Sq == 0) return SDPA_OK;
+  if (Sk == 0) return SDPA_ERR_INVALID_ARG;  // softmax over no keys
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+  Opts opt;
+  if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
+  return fwd_launch(q, k, v, out, lse, B, H, Sq, Sk, D, dropout_p, is_causal, scale, seed, offset,
+                    opt, nullptr, nullptr, 0, stream);
+}
+
+sdpa_status sdpa_fwd_varlen(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                            const sdpa_varlen* seqs, double dropout_p, int is_causal, float scale,
+                            uint64_t seed, uint64_t offset, sdpa_tensor* out, float* lse,
+                            const sdpa_options* options, sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  sdpa_status s = check_dims(q, k, v);
+  if (s != SDPA_OK) return s;
+  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
+  const int64_t H = q->size[1], Tq = q->size[2], Tk = k->size[2], D = q->size[3];
+  if ((s = check_varlen(seqs, q, k)) != SDPA_OK) return s;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if ((s = check_tensor(q, 1, H, Tq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(k, 1, H, Tk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(v, 1, H, Tk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(out, 1, H, Tq, D)) != SDPA_OK) return s;
+  if (H * Tq == 0) return SDPA_OK;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+  if (options && (options->attn_bias || options->dbias)) return SDPA_ERR_UNSUPPORTED;
+  const int64_t B = seqs->batch, Mq = seqs->max_seqlen_q, Mk = seqs->max_seqlen_k;
+  Opts opt;
+  if ((s = resolve_options(options, B, H, Mq, Mk, &opt)) != SDPA_OK) return s;
+  return fwd_launch(q, k, v, out, lse, B, H, Mq, Mk, D, dropout_p, is_causal, scale, seed, offset,
+                    opt, seqs->cu_seqlens_q, seqs->cu_seqlens_k, Tq, stream);
 }
 
 sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
@@ -391,106 +577,9 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
   Opts opt;
   if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
-  const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return SDPA_ERR_WORKSPACE;
-
-  // workspace: [dQ accumulator | per-key-tile dQ partials (deterministic)], lse2, delta
-  const int64_t Sq_pad = round_up(Sq, 128);
-  const int64_t n_kv = (Sk + 127) / 128;
-  const int64_t slice = B * H * Sq_pad * Dk;
-  float* dq_region = static_cast<float*>(workspace);
-  float* lse2 = dq_region + slice * (opt.det ? n_kv : 1);
-  float* delta = lse2 + B * H * Sq_pad;
-  float* dq_acc = opt.det ? nullptr : dq_region;
-
-  const uint32_t mq = static_cast<uint32_t>(8192 / Dk);
-  CUtensorMap maps[6];
-  if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
-      !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
-    return SDPA_ERR_CUDA;
-
-  uint32_t* err = error_word();
-  if (!err) return SDPA_ERR_CUDA;
-
-  PreParams pp;
-  pp.B = static_cast<int>(B);
-  pp.H = static_cast<int>(H);
-  pp.Sq = static_cast<int>(Sq);
-  pp.Sq_pad = static_cast<int>(Sq_pad);
-  pp.D = static_cast<int>(Dk);
-  pp.D_io = static_cast<int>(D);
-  pp.out = strided(out);
-  pp.dout = strided(dout);
-  pp.lse = lse;
-  pp.lse2 = lse2;
-  pp.delta = delta;
-  pp.dq_acc = dq_acc;
-  cudaError_t e = launch_bwd_preprocess(pp, stream);
-  if (e != cudaSuccess) return SDPA_ERR_CUDA;
-
-  BwdParams p;
-  p.B = pp.B;
-  p.H = pp.H;
-  p.Sq = pp.Sq;
-  p.Sk = static_cast<int>(Sk);
-  p.Sq_pad = pp.Sq_pad;
-  p.n_kv_tiles = static_cast<int>((Sk + 127) / 128);
-  p.scale_log2 = scale * kLog2e;
-  p.scale = scale;
-  p.drop_threshold = drop_threshold(dropout_p);
-  p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
-  p.pk = philox_key(seed, offset);
-  p.rng_dev = opt.rng;
-  p.b0 = opt.b0;
-  p.h0 = opt.h0;
-  p.H_total = opt.H_total;
-  p.bias = opt.bias;
-  p.dbias = opt.dbias;
-  p.h_major = (opt.bias.data != nullptr && opt.bias.sB == 0 && B > 1) ? 1 : 0;
-  p.dq_acc = dq_acc;
-  p.dq_part = opt.det ? dq_region : nullptr;
-  p.part_stride = static_cast<size_t>(slice);
-  p.lse2 = lse2;
-  p.delta = delta;
-  p.err = err;
-  p.wait_limit_ns = wait_limit_ns();
-  if (opt.dbias.data != nullptr && is_causal) {
-    // key tiles above the diagonal are never visited: their dbias is 0
-    e = launch_dbias_zero_causal(opt.dbias, static_cast<int>(B), static_cast<int>(H),
-                                 static_cast<int>(Sq), static_cast<int>(Sk), stream);
-    if (e != cudaSuccess) return SDPA_ERR_CUDA;
-  }
-  e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
-  if (e != cudaSuccess) return SDPA_ERR_CUDA;
-
-  if (opt.det) {
-    SumParams sp;
-    sp.B = pp.B;
-    sp.H = pp.H;
-    sp.Sq = pp.Sq;
-    sp.Sq_pad = pp.Sq_pad;
-    sp.D = pp.D;
-    sp.D_io = pp.D_io;
-    sp.n_kv_tiles = p.n_kv_tiles;
-    sp.causal = is_causal != 0;
-    sp.scale = scale;
-    sp.dq_part = dq_region;
-    sp.part_stride = static_cast<size_t>(slice);
-    sp.dq = strided(dq);
-    return finish(launch_bwd_dq_sum(sp, stream), stream);
-  }
-  ConvParams cp;
-  cp.B = pp.B;
-  cp.H = pp.H;
-  cp.Sq = pp.Sq;
-  cp.Sq_pad = pp.Sq_pad;
-  cp.D = pp.D;
-  cp.D_io = pp.D_io;
-  cp.scale = scale;
-  cp.dq_acc = dq_acc;
-  cp.dq = strided(dq);
-  return finish(launch_bwd_dq_convert(cp, stream), stream);
+  return bwd_launch(dout, q, k, v, out, lse, B, H, Sq, Sk, D, dropout_p, is_causal, seed, offset,
+                    scale, dq, dk, dv, workspace, workspace_bytes, options, opt, nullptr, nullptr, 0,
+                    stream);
 }
 
 sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
@@ -500,6 +589,46 @@ sdpa_status sdpa_bwd(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_t
                      void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
   return sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p, is_causal, seed, offset, scale, dq, dk,
                      dv, workspace, workspace_bytes, nullptr, stream);
+}
+
+size_t sdpa_bwd_varlen_workspace_size(const sdpa_varlen* seqs, int64_t H, int64_t D,
+                                      const sdpa_options* options) {
+  if (!seqs) return 0;
+  return sdpa_bwd_workspace_size_ex(seqs->batch, H, seqs->max_seqlen_q, seqs->max_seqlen_k, D,
+                                    options);
+}
+
+sdpa_status sdpa_bwd_varlen(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
+                            const sdpa_tensor* v, const sdpa_tensor* out, const float* lse,
+                            const sdpa_varlen* seqs, double dropout_p, int is_causal,
+                            uint64_t seed, uint64_t offset, float scale, sdpa_tensor* dq,
+                            sdpa_tensor* dk, sdpa_tensor* dv, void* workspace,
+                            size_t workspace_bytes, const sdpa_options* options,
+                            sdpa_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  sdpa_status s = check_dims(q, k, v);
+  if (s != SDPA_OK) return s;
+  if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
+  const int64_t H = q->size[1], Tq = q->size[2], Tk = k->size[2], D = q->size[3];
+  if ((s = check_varlen(seqs, q, k)) != SDPA_OK) return s;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if ((s = check_tensor(q, 1, H, Tq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(k, 1, H, Tk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(v, 1, H, Tk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dout, 1, H, Tq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(out, 1, H, Tq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dq, 1, H, Tq, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dk, 1, H, Tk, D)) != SDPA_OK) return s;
+  if ((s = check_tensor(dv, 1, H, Tk, D)) != SDPA_OK) return s;
+  if (H == 0 || Tk == 0) return SDPA_OK;  // no keys: nothing to write
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
+  if (options && (options->attn_bias || options->dbias)) return SDPA_ERR_UNSUPPORTED;
+  const int64_t B = seqs->batch, Mq = seqs->max_seqlen_q, Mk = seqs->max_seqlen_k;
+  Opts opt;
+  if ((s = resolve_options(options, B, H, Mq, Mk, &opt)) != SDPA_OK) return s;
+  return bwd_launch(dout, q, k, v, out, lse, B, H, Mq, Mk, D, dropout_p, is_causal, seed, offset,
+                    scale, dq, dk, dv, workspace, workspace_bytes, options, opt,
+                    seqs->cu_seqlens_q, seqs->cu_seqlens_k, Tq, stream);
 }
 
 sdpa_status sdpa_dropout_mask_debug_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk,

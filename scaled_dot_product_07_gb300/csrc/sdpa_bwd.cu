@@ -38,10 +38,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const PreParams p) 
     const int i = static_cast<int>(row - bh * p.Sq_pad);
     const int b = static_cast<int>(bh / p.H);
     const int h = static_cast<int>(bh - static_cast<int64_t>(b) * p.H);
+    // row i of sequence b: the problem's row, or packed row qs + i
+    int len = p.Sq, qs = 0, tb = b;
+    if (p.cu_q != nullptr) {
+      qs = p.cu_q[b];
+      len = p.cu_q[b + 1] - qs;
+      tb = 0;
+    }
     float acc = 0.f;
-    if (i < p.Sq && part * 8 < p.D_io) {  // columns past D_io are the kernels' zero padding
-      const int64_t eo = b * p.out.sB + h * p.out.sH + i * p.out.sS + part * 8;
-      const int64_t ed = b * p.dout.sB + h * p.dout.sH + i * p.dout.sS + part * 8;
+    if (i < len && part * 8 < p.D_io) {  // columns past D_io are the kernels' zero padding
+      const int64_t eo = tb * p.out.sB + h * p.out.sH + static_cast<int64_t>(qs + i) * p.out.sS + part * 8;
+      const int64_t ed =
+          tb * p.dout.sB + h * p.dout.sH + static_cast<int64_t>(qs + i) * p.dout.sS + part * 8;
       const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.out.data) + eo);
       const uint4 d = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dout.data) + ed);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
@@ -63,7 +71,9 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const PreParams p) 
     }
     if (part == 0) {
       p.delta[row] = acc;
-      p.lse2[row] = i < p.Sq ? p.lse[bh * p.Sq + i] * kLog2e : INFINITY;
+      const size_t li = p.cu_q != nullptr ? static_cast<size_t>(h) * p.total_q + qs + i
+                                          : static_cast<size_t>(bh) * p.Sq + i;
+      p.lse2[row] = i < len ? p.lse[li] * kLog2e : INFINITY;
     }
   }
 }
@@ -81,6 +91,12 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p)
     const int i = static_cast<int>(row - bh * p.Sq);
     const int b = static_cast<int>(bh / p.H);
     const int h = static_cast<int>(bh - static_cast<int64_t>(b) * p.H);
+    int qs = 0, tb = b;
+    if (p.cu_q != nullptr) {  // packed: rows past the sequence's length do not exist
+      qs = p.cu_q[b];
+      if (i >= p.cu_q[b + 1] - qs) continue;
+      tb = 0;
+    }
     const float4* src =
         reinterpret_cast<const float4*>(p.dq_acc + (bh * p.Sq_pad + i) * p.D + part * 8);
     const float4 a = src[0], c = src[1];
@@ -89,7 +105,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p)
     o.y = pack_bf16x2(a.z * p.scale, a.w * p.scale);
     o.z = pack_bf16x2(c.x * p.scale, c.y * p.scale);
     o.w = pack_bf16x2(c.z * p.scale, c.w * p.scale);
-    const int64_t e = b * p.dq.sB + h * p.dq.sH + i * p.dq.sS + part * 8;
+    const int64_t e = tb * p.dq.sB + h * p.dq.sH + static_cast<int64_t>(qs + i) * p.dq.sS + part * 8;
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq.data) + e) = o;
   }
 }
@@ -110,7 +126,14 @@ __global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
     const int i = static_cast<int>(row - bh * p.Sq);
     const int b = static_cast<int>(bh / p.H);
     const int h = static_cast<int>(bh - static_cast<int64_t>(b) * p.H);
-    const int k_last = p.causal ? min(p.n_kv_tiles - 1, i / 128) : p.n_kv_tiles - 1;
+    int qs = 0, tb = b, n_kv = p.n_kv_tiles;
+    if (p.cu_q != nullptr) {  // packed: this sequence's rows and key tiles only
+      qs = p.cu_q[b];
+      if (i >= p.cu_q[b + 1] - qs) continue;
+      n_kv = (p.cu_k[b + 1] - p.cu_k[b] + 127) / 128;
+      tb = 0;
+    }
+    const int k_last = p.causal ? min(n_kv - 1, i / 128) : n_kv - 1;
     const float* src = p.dq_part + (bh * p.Sq_pad + i) * p.D + part * 8;
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k <= k_last; ++k) {
@@ -124,7 +147,7 @@ __global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
     o.y = pack_bf16x2(a[2] * p.scale, a[3] * p.scale);
     o.z = pack_bf16x2(a[4] * p.scale, a[5] * p.scale);
     o.w = pack_bf16x2(a[6] * p.scale, a[7] * p.scale);
-    const int64_t e = b * p.dq.sB + h * p.dq.sH + i * p.dq.sS + part * 8;
+    const int64_t e = tb * p.dq.sB + h * p.dq.sH + static_cast<int64_t>(qs + i) * p.dq.sS + part * 8;
     *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq.data) + e) = o;
   }
 }
@@ -254,7 +277,7 @@ __device__ __forceinline__ void store_row_bf16_sw128(uint32_t base, int row, con
   }
 }
 
-template <int D, bool CAUSAL, bool DROPOUT, bool BIAS>
+template <int D, bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -296,7 +319,17 @@ __global__ void __launch_bounds__(320, 1)
   const int h = p.h_major ? slot / p.B : slot - b * p.H;
   const int bh = b * p.H + h;
   const int k0 = kv_tile * 128;
-  const int n_qt = (p.Sq + MQ - 1) / MQ;
+  // the sequence: the whole [Sq, Sk] problem, or sequence b of a packed batch
+  int Sq = p.Sq, Sk = p.Sk, qs = 0, ks = 0;
+  if (VARLEN) {
+    qs = p.cu_q[b];
+    Sq = p.cu_q[b + 1] - qs;
+    ks = p.cu_k[b];
+    Sk = p.cu_k[b + 1] - ks;
+    if (k0 >= Sk) return;  // no keys of the sequence in this tile
+  }
+  const int tb = VARLEN ? 0 : b;  // batch coordinate in the tensor maps
+  const int n_qt = (Sq + MQ - 1) / MQ;
   const int qt_first = CAUSAL ? min(k0 / MQ, n_qt) : 0;
   const int n_steps = n_qt - qt_first;
 
@@ -336,8 +369,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::kKvBytes);
 #pragma unroll
       for (int s = 0; s < D / 64; ++s) {
-        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, k0, h, b);
-        tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, k0, h, b);
+        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, ks + k0, h, tb);
+        tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, ks + k0, h, tb);
       }
       for (int t = 0; t < n_steps; ++t) {
         const int st = t % S;
@@ -347,9 +380,9 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s) {
           tma_load_4d(smem + L::kQ + st * L::kQBytes + s * L::kQSlab, &tm_q, &q_full[st], s * 64,
-                      i0, h, b);
+                      qs + i0, h, tb);
           tma_load_4d(smem + L::kDO + st * L::kQBytes + s * L::kQSlab, &tm_do, &q_full[st],
-                      s * 64, i0, h, b);
+                      s * 64, qs + i0, h, tb);
         }
         const size_t vec = static_cast<size_t>(bh) * p.Sq_pad + i0;
         bulk_load(smem + L::kLse + st * MQ * 4, p.lse2 + vec, MQ * 4, &q_full[st]);
@@ -453,7 +486,7 @@ __global__ void __launch_bounds__(320, 1)
       const int i0 = (qt_first + t) * MQ;
       const uint32_t lse_s = sb + L::kLse + st * MQ * 4;
       const uint32_t del_s = sb + L::kDelta + st * MQ * 4;
-      const bool key_ok = kj < p.Sk;
+      const bool key_ok = kj < Sk;
       const uint16_t* bp = BIAS ? p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0)
                                 : nullptr;
       mbar_wait(&q_full[st], (t / S) & 1, wc, kSiteBwdQFull);
@@ -461,9 +494,9 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float pv[MQ];
       tmem_load_row<MQ>(tS, pv);
-      const bool need_mask = (k0 + 128 > p.Sk) || (CAUSAL && i0 < k0 + 127);
+      const bool need_mask = (k0 + 128 > Sk) || (CAUSAL && i0 < k0 + 127);
       // visible query rows of this key: qi >= kj (causal) and the key exists
-      const int first_vis = kj >= p.Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
+      const int first_vis = kj >= Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
 #pragma unroll
       for (int cc = 0; cc < MQ / 32; ++cc) {
         uint32_t bpk[16];  // bias of query rows i0 + 32cc .. +32 at key kj, bf16 pairs
@@ -472,8 +505,8 @@ __global__ void __launch_bounds__(320, 1)
           for (int c2 = 0; c2 < 16; ++c2) {
             const int ia = i0 + 32 * cc + 2 * c2;
             const uint32_t lo =
-                (key_ok && ia < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
-            const uint32_t hi = (key_ok && ia + 1 < p.Sq)
+                (key_ok && ia < Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
+            const uint32_t hi = (key_ok && ia + 1 < Sq)
                                     ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS)
                                     : 0u;
             bpk[c2] = lo | (hi << 16);
@@ -495,12 +528,12 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int w = 0; w < MQ / 32; ++w) kb[w] = 0xffffffffu;
       if (DROPOUT) {
-        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + i0) *
-                                    static_cast<uint64_t>(p.Sk) +
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
+                                    static_cast<uint64_t>(p.Sk_ctr) +
                                 kj;
 #pragma unroll
         for (int c = 0; c < MQ; ++c) {
-          const bool kp = keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, pk);
+          const bool kp = keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
           if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
         }
       }
@@ -540,7 +573,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int qi = i0 + cc * 32 + i;
-            if (qi < p.Sq)
+            if (qi < Sq)
               dp[static_cast<int64_t>(qi) * p.dbias.sS] =
                   static_cast<uint16_t>(pack_bf16x2(ds[i], 0.f) & 0xffffu);
           }
@@ -620,6 +653,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t acc = tmem + (is_dv ? L::kTmemDV : L::kTmemDK) + lane_base;
     const uint32_t stage = sb + (is_dv ? L::kK : L::kV);  // K/V tiles are dead after `done`
     const float mul = is_dv ? 1.f : p.scale;
+    // a packed sequence's last key tile is stored row by row, so that rows
+    // of the next sequence are never written (uniform over the CTA)
+    const bool direct = VARLEN && (k0 + 128 > Sk);
     if (n_steps > 0) {
       mbar_wait(done, 0, wc, kSiteBwdDone);
       tc_fence_after();
@@ -640,22 +676,34 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int col0 = c * 32 + q4 * 8;
-        st_shared_v4(stage + (col0 >> 6) * L::kKvSlab + sw128_offset(r, (col0 & 63) >> 3),
-                     pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]),
-                     pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                     pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
-                     pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
+        const uint32_t w0 = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
+        const uint32_t w1 = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
+        const uint32_t w2 = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
+        const uint32_t w3 = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
+        if (direct) {
+          if (k0 + r < Sk && col0 < p.D_io) {
+            const StridedBf16& o = is_dv ? p.dv_io : p.dk_io;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(o.data) + h * o.sH +
+                                      static_cast<int64_t>(ks + k0 + r) * o.sS + col0) =
+                make_uint4(w0, w1, w2, w3);
+          }
+        } else {
+          st_shared_v4(stage + (col0 >> 6) * L::kKvSlab + sw128_offset(r, (col0 & 63) >> 3), w0,
+                       w1, w2, w3);
+        }
       }
     }
-    fence_async_smem();
-    named_barrier_sync(is_dv ? 3 : 4, 128);
-    if (r == 0) {
+    if (!direct) {
+      fence_async_smem();
+      named_barrier_sync(is_dv ? 3 : 4, 128);
+      if (r == 0) {
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
-                     s * 64, k0, h, b);
-      bulk_commit();
-      bulk_wait_all();
+        for (int s = 0; s < D / 64; ++s)
+          tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
+                       s * 64, ks + k0, h, tb);
+        bulk_commit();
+        bulk_wait_all();
+      }
     }
   }
 
@@ -667,11 +715,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool C, bool DR, bool BI>
+template <int D, bool C, bool DR, bool BI, bool VL>
 cudaError_t launch_bwd_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_main_kernel<D, C, DR, BI>;
+  auto kern = bwd_main_kernel<D, C, DR, BI, VL>;
   const int smem = BwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<bwd_main_kernel<D, C, DR, BI>>(smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel<D, C, DR, BI, VL>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, 320, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
@@ -725,10 +773,12 @@ cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStre
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout, const CUtensorMap* maps,
                             const BwdParams& p, cudaStream_t stream) {
   const bool bias = p.bias.data != nullptr;
+  const bool varlen = p.cu_q != nullptr;  // packed batches take no bias
 #define SDPA_BWD_CASE(DD, CC, RR)                                                    \
   if (D == DD && causal == CC && dropout == RR)                                      \
-    return bias ? launch_bwd_t<DD, CC, RR, true>(maps, p, stream)                    \
-                : launch_bwd_t<DD, CC, RR, false>(maps, p, stream);
+    return varlen ? launch_bwd_t<DD, CC, RR, false, true>(maps, p, stream)           \
+                  : (bias ? launch_bwd_t<DD, CC, RR, true, false>(maps, p, stream)   \
+                          : launch_bwd_t<DD, CC, RR, false, false>(maps, p, stream));
   SDPA_BWD_CASE(64, false, false)
   SDPA_BWD_CASE(64, false, true)
   SDPA_BWD_CASE(64, true, false)

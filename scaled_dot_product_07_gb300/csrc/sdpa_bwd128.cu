@@ -71,7 +71,7 @@ __device__ __forceinline__ void touch32(uint32_t (&r)[32]) {
                  "+r"(r[30]), "+r"(r[31]));
 }
 
-template <bool CAUSAL, bool DROPOUT, bool BIAS>
+template <bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
 __global__ void __launch_bounds__(448, 1)
     bwd_main_kernel_d128(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -114,7 +114,17 @@ __global__ void __launch_bounds__(448, 1)
   const int h = p.h_major ? slot / p.B : slot - b * p.H;
   const int bh = b * p.H + h;
   const int k0 = kv_tile * 128;
-  const int n_qt = (p.Sq + MQ - 1) / MQ;
+  // the sequence: the whole [Sq, Sk] problem, or sequence b of a packed batch
+  int Sq = p.Sq, Sk = p.Sk, qs = 0, ks = 0;
+  if (VARLEN) {
+    qs = p.cu_q[b];
+    Sq = p.cu_q[b + 1] - qs;
+    ks = p.cu_k[b];
+    Sk = p.cu_k[b + 1] - ks;
+    if (k0 >= Sk) return;  // no keys of the sequence in this tile
+  }
+  const int tb = VARLEN ? 0 : b;  // batch coordinate in the tensor maps
+  const int n_qt = (Sq + MQ - 1) / MQ;
   const int qt_first = CAUSAL ? min(k0 / MQ, n_qt) : 0;
   const int n_steps = n_qt - qt_first;
 
@@ -156,8 +166,8 @@ __global__ void __launch_bounds__(448, 1)
       mbar_arrive_expect_tx(kv_full, 2 * L::kKvBytes);
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
-        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, k0, h, b);
-        tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, k0, h, b);
+        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, ks + k0, h, tb);
+        tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, ks + k0, h, tb);
       }
       for (int t = 0; t < n_steps; ++t) {
         const int st = t % NS;
@@ -167,9 +177,9 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           tma_load_4d(smem + L::kQ + st * L::kQBytes + s * L::kQSlab, &tm_q, &q_full[st], s * 64,
-                      i0, h, b);
+                      qs + i0, h, tb);
           tma_load_4d(smem + L::kDO + st * L::kQBytes + s * L::kQSlab, &tm_do, &q_full[st],
-                      s * 64, i0, h, b);
+                      s * 64, qs + i0, h, tb);
         }
         const size_t vec = static_cast<size_t>(bh) * p.Sq_pad + i0;
         bulk_load(smem + L::kLse + st * MQ * 4, p.lse2 + vec, MQ * 4, &q_full[st]);
@@ -282,15 +292,15 @@ __global__ void __launch_bounds__(448, 1)
       // fetched before the waits so that its latency is hidden
       uint32_t bpk[MQ / 2];
       if (BIAS) {
-        const bool key_ok = kj < p.Sk;
+        const bool key_ok = kj < Sk;
         const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0);
 #pragma unroll
         for (int c2 = 0; c2 < MQ / 2; ++c2) {
           const int ia = i0 + 2 * c2;
           const uint32_t lo =
-              (key_ok && ia < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
+              (key_ok && ia < Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
           const uint32_t hi =
-              (key_ok && ia + 1 < p.Sq) ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS) : 0u;
+              (key_ok && ia + 1 < Sq) ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS) : 0u;
           bpk[c2] = lo | (hi << 16);
         }
       }
@@ -310,8 +320,8 @@ __global__ void __launch_bounds__(448, 1)
           pv[32 + c] = __uint_as_float(r1[c]);
         }
       }
-      const bool need_mask = (k0 + 128 > p.Sk) || (CAUSAL && i0 < k0 + 127);
-      const int first_vis = kj >= p.Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
+      const bool need_mask = (k0 + 128 > Sk) || (CAUSAL && i0 < k0 + 127);
+      const int first_vis = kj >= Sk ? (1 << 30) : (CAUSAL ? kj - i0 : 0);
 #pragma unroll
       for (int c = 0; c < MQ; ++c) {
         float arg = fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4));
@@ -324,13 +334,13 @@ __global__ void __launch_bounds__(448, 1)
       }
       uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
       if (DROPOUT) {
-        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + i0) *
-                                    static_cast<uint64_t>(p.Sk) +
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
+                                    static_cast<uint64_t>(p.Sk_ctr) +
                                 kj;
 #pragma unroll
         for (int c = 0; c < MQ; ++c) {
           const bool kp =
-              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk, p.drop_threshold, pk);
+              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
           if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
         }
       }
@@ -369,13 +379,13 @@ __global__ void __launch_bounds__(448, 1)
           if (DROPOUT) g = ((kb[cc] >> i) & 1u) ? g * p.drop_rescale : 0.f;
           ds[i] = pv[e] * (g - ld_shared_f32(del_s + e * 4));
         }
-        if (BIAS && p.dbias.data != nullptr && kj < p.Sk) {
+        if (BIAS && p.dbias.data != nullptr && kj < Sk) {
           // dbias(i, kj) = dS(i, kj); a warp writes 64 contiguous bytes per row
           uint16_t* dp = p.dbias.data + b * p.dbias.sB + h * p.dbias.sH + kj;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int qi = i0 + cc * 32 + i;
-            if (qi < p.Sq)
+            if (qi < Sq)
               dp[static_cast<int64_t>(qi) * p.dbias.sS] =
                   static_cast<uint16_t>(pack_bf16x2(ds[i], 0.f) & 0xffffu);
           }
@@ -439,6 +449,9 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t acc = tmem + (is_dv ? L::kTmemDV : L::kTmemDK) + lane_base;
     const uint32_t stage = sb + (is_dv ? L::kK : L::kV);  // K/V tiles are dead after `done`
     const float mul = is_dv ? 1.f : p.scale;
+    // a packed sequence's last key tile is stored row by row, so that rows
+    // of the next sequence are never written (uniform over the CTA)
+    const bool direct = VARLEN && (k0 + 128 > Sk);
     if (n_steps > 0) {
       mbar_wait(done, 0, wc, kSiteBwdDone);
       tc_fence_after();
@@ -459,22 +472,34 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int col0 = c * 32 + q4 * 8;
-        st_shared_v4(stage + (col0 >> 6) * L::kKvSlab + sw128_offset(r, (col0 & 63) >> 3),
-                     pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]),
-                     pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]),
-                     pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]),
-                     pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]));
+        const uint32_t w0 = pack_bf16x2(v[q4 * 8 + 0], v[q4 * 8 + 1]);
+        const uint32_t w1 = pack_bf16x2(v[q4 * 8 + 2], v[q4 * 8 + 3]);
+        const uint32_t w2 = pack_bf16x2(v[q4 * 8 + 4], v[q4 * 8 + 5]);
+        const uint32_t w3 = pack_bf16x2(v[q4 * 8 + 6], v[q4 * 8 + 7]);
+        if (direct) {
+          if (k0 + r < Sk && col0 < p.D_io) {
+            const StridedBf16& o = is_dv ? p.dv_io : p.dk_io;
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(o.data) + h * o.sH +
+                                      static_cast<int64_t>(ks + k0 + r) * o.sS + col0) =
+                make_uint4(w0, w1, w2, w3);
+          }
+        } else {
+          st_shared_v4(stage + (col0 >> 6) * L::kKvSlab + sw128_offset(r, (col0 & 63) >> 3), w0,
+                       w1, w2, w3);
+        }
       }
     }
-    fence_async_smem();
-    named_barrier_sync(is_dv ? 3 : 4, 128);
-    if (r == 0) {
+    if (!direct) {
+      fence_async_smem();
+      named_barrier_sync(is_dv ? 3 : 4, 128);
+      if (r == 0) {
 #pragma unroll
-      for (int s = 0; s < 2; ++s)
-        tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
-                     s * 64, k0, h, b);
-      bulk_commit();
-      bulk_wait_all();
+        for (int s = 0; s < 2; ++s)
+          tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
+                       s * 64, ks + k0, h, tb);
+        bulk_commit();
+        bulk_wait_all();
+      }
     }
   }
 
@@ -486,11 +511,11 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
-template <bool C, bool DR, bool BI>
+template <bool C, bool DR, bool BI, bool VL>
 cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_main_kernel_d128<C, DR, BI>;
+  auto kern = bwd_main_kernel_d128<C, DR, BI, VL>;
   const int smem = B128::kAlloc;
-  cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR, BI>>(smem);
+  cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR, BI, VL>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, B128::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
@@ -503,16 +528,22 @@ size_t bwd_d128_smem_bytes() { return B128::kAlloc; }
 
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout, const CUtensorMap* maps,
                                  const BwdParams& p, cudaStream_t stream) {
-  if (p.bias.data != nullptr) {
-    if (causal && dropout) return launch_t<true, true, true>(maps, p, stream);
-    if (causal) return launch_t<true, false, true>(maps, p, stream);
-    if (dropout) return launch_t<false, true, true>(maps, p, stream);
-    return launch_t<false, false, true>(maps, p, stream);
+  if (p.cu_q != nullptr) {  // packed batch (no bias)
+    if (causal && dropout) return launch_t<true, true, false, true>(maps, p, stream);
+    if (causal) return launch_t<true, false, false, true>(maps, p, stream);
+    if (dropout) return launch_t<false, true, false, true>(maps, p, stream);
+    return launch_t<false, false, false, true>(maps, p, stream);
   }
-  if (causal && dropout) return launch_t<true, true, false>(maps, p, stream);
-  if (causal) return launch_t<true, false, false>(maps, p, stream);
-  if (dropout) return launch_t<false, true, false>(maps, p, stream);
-  return launch_t<false, false, false>(maps, p, stream);
+  if (p.bias.data != nullptr) {
+    if (causal && dropout) return launch_t<true, true, true, false>(maps, p, stream);
+    if (causal) return launch_t<true, false, true, false>(maps, p, stream);
+    if (dropout) return launch_t<false, true, true, false>(maps, p, stream);
+    return launch_t<false, false, true, false>(maps, p, stream);
+  }
+  if (causal && dropout) return launch_t<true, true, false, false>(maps, p, stream);
+  if (causal) return launch_t<true, false, false, false>(maps, p, stream);
+  if (dropout) return launch_t<false, true, false, false>(maps, p, stream);
+  return launch_t<false, false, false, false>(maps, p, stream);
 }
 
 }  // namespace sdpa

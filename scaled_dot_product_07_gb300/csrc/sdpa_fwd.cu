@@ -82,7 +82,7 @@ __device__ __forceinline__ int kv_tiles_for(int r0, int Sq, int Sk, bool causal)
   return min(n, min(r0 + 127, Sq - 1) / 128 + 1);
 }
 
-template <int D, bool CAUSAL, bool DROPOUT, bool BIAS>
+template <int D, bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -121,8 +121,27 @@ __global__ void __launch_bounds__(320, 1)
   const int h = p.h_major ? slot / p.B : slot - b * p.H;
   const int bh = b * p.H + h;
   const int q0 = pair * 256;
-  const int n_t[2] = {kv_tiles_for(q0, p.Sq, p.Sk, CAUSAL),
-                      kv_tiles_for(q0 + 128, p.Sq, p.Sk, CAUSAL)};
+  // the sequence: the whole [Sq, Sk] problem, or sequence b of a packed batch
+  int Sq = p.Sq, Sk = p.Sk, qs = 0, ks = 0;
+  if (VARLEN) {
+    qs = p.cu_q[b];
+    Sq = p.cu_q[b + 1] - qs;
+    ks = p.cu_k[b];
+    Sk = p.cu_k[b + 1] - ks;
+    if (q0 >= Sq) return;  // the sequence has no query rows in this tile pair
+    if (Sk <= 0) {
+      // no keys: the rows' outputs are 0 and their log-sum-exp is -inf
+      for (int r = threadIdx.x; r < 256 && q0 + r < Sq; r += blockDim.x) {
+        uint16_t* o = static_cast<uint16_t*>(p.out_io.data) + h * p.out_io.sH +
+                      static_cast<int64_t>(qs + q0 + r) * p.out_io.sS;
+        for (int c = 0; c < p.D_io; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+        p.lse[static_cast<size_t>(h) * p.total_q + qs + q0 + r] = -INFINITY;
+      }
+      return;
+    }
+  }
+  const int tb = VARLEN ? 0 : b;  // batch coordinate in the tensor maps
+  const int n_t[2] = {kv_tiles_for(q0, Sq, Sk, CAUSAL), kv_tiles_for(q0 + 128, Sq, Sk, CAUSAL)};
   const int n_kv = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
@@ -163,7 +182,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, &tm_q, q_full, s * 64,
-                      q0 + 128 * i, h, b);
+                      qs + q0 + 128 * i, h, tb);
       }
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % S;
@@ -174,13 +193,13 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
-                      s * 64, j * 128, h, b);
+                      s * 64, ks + j * 128, h, tb);
         if (j >= S) mbar_wait(&v_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
         mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &v_full[st],
-                      s * 64, j * 128, h, b);
+                      s * 64, ks + j * 128, h, tb);
       }
       if (*abort_word) {
         // give the loads still in flight time to land before the CTA exits
@@ -286,25 +305,25 @@ __global__ void __launch_bounds__(320, 1)
         if (BIAS) {
           // start the next key tile's bias line towards L2
           const int kn = (j + 1) * 128 + 64 * half;
-          if (j + 1 < n_t[i] && kn < p.Sk) {
+          if (j + 1 < n_t[i] && kn < Sk) {
             const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                                 static_cast<int64_t>(min(qi, p.Sq - 1)) * p.bias.sS + kn;
+                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
             prefetch_l2(np);
-            prefetch_l2(np + min(56, p.Sk - 1 - kn));
+            prefetch_l2(np + min(56, Sk - 1 - kn));
           }
           const int kb = j * 128 + 64 * half;
           const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                               static_cast<int64_t>(min(qi, p.Sq - 1)) * p.bias.sS + kb;
+                               static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            if (kb + 8 * c + 8 <= p.Sk) {
+            if (kb + 8 * c + 8 <= Sk) {
               bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
             } else {
               // key tail: only the keys that exist are read
               uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
               for (int e = 0; e < 8; ++e)
-                if (kb + 8 * c + e < p.Sk)
+                if (kb + 8 * c + e < Sk)
                   w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
               bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
@@ -337,8 +356,8 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
         const int k0 = j * 128 + 64 * half;  // first key of this half
-        if ((k0 + 64 > p.Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
-          const int lim = CAUSAL ? min(p.Sk - k0, qi - k0 + 1) : (p.Sk - k0);
+        if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
+          const int lim = CAUSAL ? min(Sk - k0, qi - k0 + 1) : (Sk - k0);
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             if (c >= lim) x[c] = -INFINITY;
@@ -376,8 +395,8 @@ __global__ void __launch_bounds__(320, 1)
 
         uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
         if (DROPOUT) {
-          const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq + qi) *
-                                 static_cast<uint64_t>(p.Sk);
+          const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + qi) *
+                                 static_cast<uint64_t>(p.Sk_ctr);
           keep_bits<2>(n_row + k0, p.drop_threshold, pk, keep);
         }
         float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
@@ -420,6 +439,9 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_row;
       const uint32_t oa = sb + L::kQ + i * L::kTileBytes;  // Q_i is dead after o_full[i]
+      // a packed sequence's last tile is stored row by row, so that rows of
+      // the next sequence are never written (uniform over the CTA)
+      const bool direct = VARLEN && (q0 + 128 * i + 128 > Sq);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns
         uint32_t o[32];
@@ -428,28 +450,36 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int col0 = (D / 2) * half + c * 32 + q4 * 8;
-          const uint32_t addr =
-              oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3);
-          st_shared_v4(addr,
-                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
-                                   __uint_as_float(o[q4 * 8 + 1]) * inv_l),
-                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
-                                   __uint_as_float(o[q4 * 8 + 3]) * inv_l),
-                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
-                                   __uint_as_float(o[q4 * 8 + 5]) * inv_l),
-                       pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
-                                   __uint_as_float(o[q4 * 8 + 7]) * inv_l));
+          const uint32_t w0 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+          const uint32_t w1 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+          const uint32_t w2 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+          const uint32_t w3 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+          if (direct) {
+            if (qi < Sq && col0 < p.D_io)
+              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out_io.data) + h * p.out_io.sH +
+                                        static_cast<int64_t>(qs + qi) * p.out_io.sS + col0) =
+                  make_uint4(w0, w1, w2, w3);
+          } else {
+            st_shared_v4(oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3),
+                         w0, w1, w2, w3);
+          }
         }
       }
-      if (half == 0 && qi < p.Sq)
-        p.lse[static_cast<size_t>(bh) * p.Sq + qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
+      if (half == 0 && qi < Sq)
+        p.lse[(VARLEN ? static_cast<size_t>(h) * p.total_q + qs : static_cast<size_t>(bh) * Sq) +
+              qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
+      if (direct) continue;
       fence_async_smem();
       named_barrier_sync(9 + i, 256);
       if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < D / 64; ++s)
           tma_store_4d(&tm_o, smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, s * 64,
-                       q0 + 128 * i, h, b);
+                       qs + q0 + 128 * i, h, tb);
         bulk_commit();
         bulk_wait_all();
       }
@@ -464,11 +494,11 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool C, bool DR, bool BI>
+template <int D, bool C, bool DR, bool BI, bool VL>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<D, C, DR, BI>;
+  auto kern = fwd_kernel<D, C, DR, BI, VL>;
   const int smem = FwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, BI>>(smem);
+  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, BI, VL>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
@@ -484,10 +514,12 @@ size_t fwd_smem_bytes(int D) {
 cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps,
                        const FwdParams& p, cudaStream_t stream) {
   const bool bias = p.bias.data != nullptr;
+  const bool varlen = p.cu_q != nullptr;  // packed batches take no bias
 #define SDPA_FWD_CASE(DD, CC, RR)                                                    \
   if (D == DD && causal == CC && dropout == RR)                                      \
-    return bias ? launch_fwd_t<DD, CC, RR, true>(maps, p, stream)                    \
-                : launch_fwd_t<DD, CC, RR, false>(maps, p, stream);
+    return varlen ? launch_fwd_t<DD, CC, RR, false, true>(maps, p, stream)           \
+                  : (bias ? launch_fwd_t<DD, CC, RR, true, false>(maps, p, stream)   \
+                          : launch_fwd_t<DD, CC, RR, false, false>(maps, p, stream));
   SDPA_FWD_CASE(64, false, false)
   SDPA_FWD_CASE(64, false, true)
   SDPA_FWD_CASE(64, true, false)
