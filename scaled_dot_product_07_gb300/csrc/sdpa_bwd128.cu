@@ -19,8 +19,10 @@
 //               accumulator with one bulk reduce-add.
 // TMEM (512 columns): dV [0,128), dK [128,256), and two step buffers
 // {S^T, dP^T} at [256,384) and [384,512). A step's dQ^T partial (M = D =
-// 128 lanes, 64 columns) overwrites its own S^T columns once dV has read
-// P~^T from them (tcgen05 MMAs of one thread execute in order).
+// 128 lanes, 64 columns) overwrites its own dP^T columns, which the compute
+// warpgroup has read before it hands over dS^T; the next S^T into the
+// buffer therefore waits only for the compute warpgroup, and the next dP^T
+// for the dQ readout.
 // MMA order per step t: S^T(t), dP^T(t), then dV, dK, dQ of step t-1, so
 // the tensor core computes the next step's products while a compute
 // warpgroup works on the current one.
@@ -227,10 +229,12 @@ __global__ void __launch_bounds__(448, 1)
           mma_bf16_ss_if(leader, tmem + L::kTmemDK, sdesc_add(d_ds, kk * 32),
                          sdesc_add(d_qmn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
         // dQ^T [D x MQ] = K^T dS^T: A = K tile MN-major, B = dS^T MN-major; it
-        // overwrites this step's S^T columns (dV has read P~^T from them)
+        // overwrites this step's dP^T columns (the compute warpgroup read them
+        // before it signalled ds_full), so that the next S^T into this buffer
+        // need not wait for the dQ^T readout
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss_if(leader, tmem + L::tmem_s(x), sdesc_add(kd_kmn, kk * 2048),
+          mma_bf16_ss_if(leader, tmem + L::tmem_dp(x), sdesc_add(kd_kmn, kk * 2048),
                          sdesc_add(d_dsmn, kk * 2048), kIdQ, kk > 0 ? 1u : 0u);
         mma_commit_if(leader, &dq_full[x]);
         mma_commit_if(leader, &q_empty[st]);
@@ -243,11 +247,8 @@ __global__ void __launch_bounds__(448, 1)
         const uint64_t d_q = sdesc_sw128(sb + L::kQ + st * L::kQBytes, 16, 1024);
         const uint64_t d_o = sdesc_sw128(sb + L::kDO + st * L::kQBytes, 16, 1024);
         mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
-        if (t >= 2) {
-          // step buffer x: scores read by its compute warpgroup, dQ^T(t-2) read out
-          mbar_wait(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
-          mbar_wait(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
-        }
+        // step buffer x: S^T(t-2) and dP^T(t-2) read by the compute warpgroup
+        if (t >= 2) mbar_wait(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
         tc_fence_after();
         // S^T = K Q^T and dP~^T = V dO^T  (M = 128 keys, N = MQ, K = D)
 #pragma unroll
@@ -258,6 +259,11 @@ __global__ void __launch_bounds__(448, 1)
                          kIdSP, kk > 0 ? 1u : 0u);
         }
         mma_commit_if(leader, &s_full[x]);
+        // the dP^T columns held dQ^T(t-2) until the dQ warpgroup read it out
+        if (t >= 2) {
+          mbar_wait(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
+          tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
@@ -416,8 +422,8 @@ __global__ void __launch_bounds__(448, 1)
       mbar_wait(&dq_full[x], (t >> 1) & 1, wc, kSiteBwdDqFull);
       tc_fence_after();
       uint32_t r0[32], r1[32];
-      tmem_ld32(tmem + L::tmem_s(x) + lane_base, r0);
-      tmem_ld32(tmem + L::tmem_s(x) + lane_base + 32, r1);
+      tmem_ld32(tmem + L::tmem_dp(x) + lane_base, r0);
+      tmem_ld32(tmem + L::tmem_dp(x) + lane_base + 32, r1);
       tmem_ld_wait(r0);
       touch32(r1);
       tc_fence_before();
