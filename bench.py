@@ -446,49 +446,62 @@ def bench_ours(args, w):
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
         d2h = sum(x.numel() * x.element_size() for x in (hout, hlse, hdq, hdk, hdv))
 
-        # Steps are pipelined over three streams through the public API: the
-        # uploads of step t+1 and the downloads of step t overlap the kernels
-        # of step t (double-buffered device tensors, ordered by events). Every
+        # Steps are pipelined over three streams through the public API, with
+        # NB sets of device tensors (ordered by events): q, k, v are uploaded
+        # before dout so that the forward starts first, out and lse are
+        # downloaded while the backward runs, and dq, dk, dv after it. Every
         # step still copies its whole input set in and its whole result out.
+        NB = 3
         up, down, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
         hres = [tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, lse, q, k, v))
-                for _ in range(2)]
+                for _ in range(NB)]
         hres[0] = (hout, hlse, hdq, hdk, hdv)
-        dins = [tuple(torch.empty_like(x, device=dev) for x in (hq, hk, hv, hdo)) for _ in range(2)]
+        dins = [tuple(torch.empty_like(x, device=dev) for x in (hq, hk, hv, hdo)) for _ in range(NB)]
         douts = [(torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
-                  torch.empty_like(v)) for _ in range(2)]
-        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "done", "out")}
-        started = [False, False]
+                  torch.empty_like(v)) for _ in range(NB)]
+        ev = {n: [torch.cuda.Event() for _ in range(NB)]
+              for n in ("qkv", "in", "fwd", "done", "out1", "out2")}
+        started = [False] * NB
 
         def e2e_step(t):
-            bsel = t & 1
+            bsel = t % NB
             di, do_, ho = dins[bsel], douts[bsel], hres[bsel]
             with torch.cuda.stream(up):
                 if started[bsel]:
-                    up.wait_event(ev["done"][bsel])  # step t-2 has finished reading di
-                for src, dst in zip((hq, hk, hv, hdo), di):
+                    up.wait_event(ev["done"][bsel])  # step t-NB has finished reading di
+                for src, dst in zip((hq, hk, hv), di[:3]):
                     dst.copy_(src, non_blocking=True)
+                ev["qkv"][bsel].record(up)
+                di[3].copy_(hdo, non_blocking=True)
                 ev["in"][bsel].record(up)
             with torch.cuda.stream(comp):
-                comp.wait_event(ev["in"][bsel])
+                comp.wait_event(ev["qkv"][bsel])
                 if started[bsel]:
-                    comp.wait_event(ev["out"][bsel])  # step t-2's results are downloaded
+                    comp.wait_event(ev["out1"][bsel])  # step t-NB's out, lse are downloaded
                 gq, gk, gv, gdo = di
                 o, l, dq_, dk_, dv_ = do_
                 _, _, s_, off_ = sdpa.sdpa_fwd(gq, gk, gv, w.dropout_p, w.is_causal, None, w.seed,
                                                w.offset, out=o, lse=l)
+                ev["fwd"][bsel].record(comp)
+                comp.wait_event(ev["in"][bsel])
+                if started[bsel]:
+                    comp.wait_event(ev["out2"][bsel])  # step t-NB's dq, dk, dv are downloaded
                 sdpa.sdpa_bwd(gdo, gq, gk, gv, o, l, w.dropout_p, w.is_causal, s_, off_, None,
                               dq=dq_, dk=dk_, dv=dv_, workspace=ws)
                 ev["done"][bsel].record(comp)
             with torch.cuda.stream(down):
-                down.wait_event(ev["done"][bsel])
-                for src, dst in zip(do_, ho):
+                down.wait_event(ev["fwd"][bsel])
+                for src, dst in zip(do_[:2], ho[:2]):
                     dst.copy_(src, non_blocking=True)
-                ev["out"][bsel].record(down)
+                ev["out1"][bsel].record(down)
+                down.wait_event(ev["done"][bsel])
+                for src, dst in zip(do_[2:], ho[2:]):
+                    dst.copy_(src, non_blocking=True)
+                ev["out2"][bsel].record(down)
             started[bsel] = True
 
-        e2e_steps = max(4, min(args.steps, 12))
-        for t in range(2):
+        e2e_steps = max(6, min(args.steps, 40))
+        for t in range(NB):
             e2e_step(t)
         torch.cuda.synchronize()
         if world > 1:
