@@ -192,7 +192,7 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  *     contiguous (stride[3] == 1), other strides multiples of 8 elements and
  *     the base 16-byte aligned. Pass the same bias to sdpa_bwd_ex.
  *   dbias: sdpa_bwd_ex only. NULL, or a bfloat16 [B, H, Sq, Sk] tensor
- *     (keys contiguous) that receives dB = dS, the gradient of the loss with
+ *     (keys contiguous, aligned as attn_bias) that receives dB = dS, the gradient of the loss with
  *     respect to the biased scores, for every (b, h); positions hidden by
  *     the causal mask get 0. Summing it over a shared dim gives the gradient
  *     of a shared bias. Requires attn_bias.

@@ -359,7 +359,9 @@ def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if dbias is True:
-        dbias = torch.empty((B, H, Sq, Sk), dtype=torch.bfloat16, device=q.device)
+        # key rows padded to 8 elements: the gradient tiles are stored by TMA
+        pad = (Sk + 7) // 8 * 8
+        dbias = torch.empty((B, H, Sq, pad), dtype=torch.bfloat16, device=q.device)[..., :Sk]
     opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic, attn_bias,
                    dbias)
     need = int(lib.sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))

@@ -168,6 +168,29 @@ bool make_map(CUtensorMap* m, const sdpa_tensor* t, uint32_t box_rows) {
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of an attention bias [Bb, Hb, Sq, Sk] (keys contiguous) for the
+// backward's bias tiles: box [64 query rows x 128 keys], no swizzle, zeros
+// past the edges. A shared (size-1) dim is always read at coordinate 0, so
+// it gets a packed stride.
+bool make_bias_map(CUtensorMap* m, const AttnBias& bias, int64_t Bb, int64_t Hb, int64_t Sq,
+                   int64_t Sk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int64_t rowS = Sq == 1 ? (Sk + 7) / 8 * 8 : bias.sS;
+  const int64_t headS = Hb == 1 ? rowS * Sq : bias.sH;
+  const int64_t batchS = Bb == 1 ? headS * Hb : bias.sB;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(Sk), static_cast<cuuint64_t>(Sq),
+                        static_cast<cuuint64_t>(Hb), static_cast<cuuint64_t>(Bb)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(rowS * 2), static_cast<cuuint64_t>(headS * 2),
+                           static_cast<cuuint64_t>(batchS * 2)};
+  cuuint32_t box[4] = {128, 64, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(bias.data), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 PhiloxKey philox_key(uint64_t seed, uint64_t offset) {
   PhiloxKey k;
   k.k0 = static_cast<uint32_t>(seed);
@@ -203,6 +226,7 @@ struct Opts {
   int b0 = 0, h0 = 0, H_total = 0;
   bool det = false;
   AttnBias bias{nullptr, 0, 0, 0};
+  int64_t bias_B = 0, bias_H = 0;  // the bias's own batch and head extents (1 when shared)
   DBias dbias{nullptr, 0, 0, 0};
 };
 
@@ -233,7 +257,10 @@ sdpa_status check_dbias(const sdpa_tensor* t, int64_t B, int64_t H, int64_t Sq, 
   for (int d = 0; d < 4; ++d)
     if (t->stride[d] < 0) return SDPA_ERR_INVALID_ARG;
   if (Sk > 1 && t->stride[3] != 1) return SDPA_ERR_UNSUPPORTED;
-  if (reinterpret_cast<uintptr_t>(t->data) & 1u) return SDPA_ERR_ALIGNMENT;
+  // stored by TMA tiles: 16-byte aligned base and row, head, batch strides
+  if ((reinterpret_cast<uintptr_t>(t->data) & 15u) || (t->stride[0] % 8) || (t->stride[1] % 8) ||
+      (Sq > 1 && t->stride[2] % 8))
+    return SDPA_ERR_ALIGNMENT;
   *out = DBias{static_cast<uint16_t*>(t->data), t->stride[0], t->stride[1], t->stride[2]};
   return SDPA_OK;
 }
@@ -257,6 +284,8 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
     if (o->attn_bias) {
       const sdpa_status s = check_bias(o->attn_bias, B, H, Sq, Sk, &x.bias);
       if (s != SDPA_OK) return s;
+      x.bias_B = o->attn_bias->size[0];
+      x.bias_H = o->attn_bias->size[1];
     }
     if (o->dbias) {
       if (!o->attn_bias) return SDPA_ERR_INVALID_ARG;
@@ -367,9 +396,18 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   float* dq_acc = opt.det ? nullptr : dq_region;
 
   const uint32_t mq = static_cast<uint32_t>(8192 / Dk);
-  CUtensorMap maps[6];
+  CUtensorMap maps[8];  // q, k, v, dout, dk, dv, bias, dbias (copies of q's when absent)
   if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
       !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
+    return SDPA_ERR_CUDA;
+  maps[6] = maps[0];
+  maps[7] = maps[0];
+  if (opt.bias.data != nullptr &&
+      !make_bias_map(&maps[6], opt.bias, opt.bias_B, opt.bias_H, Sq, Sk))
+    return SDPA_ERR_CUDA;
+  if (opt.dbias.data != nullptr &&
+      !make_bias_map(&maps[7], AttnBias{opt.dbias.data, opt.dbias.sB, opt.dbias.sH, opt.dbias.sS},
+                     B, H, Sq, Sk))
     return SDPA_ERR_CUDA;
 
   uint32_t* err = error_word();

@@ -31,10 +31,14 @@
 namespace sdpa {
 namespace {
 
+// With an attention bias, the Q / dO ring has 2 stages instead of 3 and the
+// freed 32 KB hold the step's bias tile [64 query rows x 128 keys] (bf16,
+// unswizzled), loaded by TMA with Q and dO.
+template <bool BIAS>
 struct B128 {
   static constexpr int D = 128;
   static constexpr int kMq = 64;                 // query rows per step
-  static constexpr int kStages = 3;              // Q / dO ring
+  static constexpr int kStages = BIAS ? 2 : 3;   // Q / dO ring
   static constexpr int kKvSlab = 128 * 128;      // 128 rows x 128 bytes
   static constexpr int kKvBytes = 128 * D * 2;   // 32 KB
   static constexpr int kQSlab = kMq * 128;       // 8 KB
@@ -49,10 +53,14 @@ struct B128 {
   static constexpr int kDq = kDs + 2 * kDsBytes;
   static constexpr int kLse = kDq + kDqBytes;                // [kStages][64] fp32
   static constexpr int kDelta = kLse + kStages * kMq * 4;    // [kStages][64] fp32
-  static constexpr int kBar = kDelta + kStages * kMq * 4;
+  static constexpr int kBiasBytes = kMq * 128 * 2;            // 16 KB
+  static constexpr int kBiasT = BIAS ? (kDelta + kStages * kMq * 4 + 1023) / 1024 * 1024
+                                     : kDelta + kStages * kMq * 4;  // [kStages] tiles
+  static constexpr int kBar = kBiasT + (BIAS ? kStages * kBiasBytes : 0);
   // kv_full, q_full[S], q_empty[S], and per step buffer b in {0,1}:
   // s_full, dp_full, p_full, ds_full, sp_empty, dq_full, dq_empty, ds_empty; done
-  static constexpr int kNumBars = 1 + 2 * kStages + 8 * 2 + 1;
+  // (bias: + dbias_read[S], the dbias tile's TMA store has read its stage)
+  static constexpr int kNumBars = 1 + 2 * kStages + 8 * 2 + 1 + (BIAS ? kStages : 0);
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -80,8 +88,10 @@ __global__ void __launch_bounds__(448, 1)
                          const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_dk,
-                         const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
-  using L = B128;
+                         const __grid_constant__ CUtensorMap tm_dv,
+                         const __grid_constant__ CUtensorMap tm_bias,
+                         const __grid_constant__ CUtensorMap tm_dbias, const BwdParams p) {
+  using L = B128<BIAS>;
   constexpr int NS = L::kStages;
   constexpr int MQ = L::kMq;
   extern __shared__ uint8_t smem_raw[];
@@ -102,6 +112,7 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* dq_empty = dq_full + 2;
   uint64_t* ds_empty = dq_empty + 2;
   uint64_t* done = ds_empty + 2;
+  uint64_t* dbias_read = done + 1;  // [NS], bias only
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
 
@@ -147,6 +158,8 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&ds_empty[x], 1);
     }
     mbar_init(done, 1);
+    if (BIAS)
+      for (int s = 0; s < NS; ++s) mbar_init(&dbias_read[s], 1);
     *abort_word = 0u;
     fence_mbar_init();
   }
@@ -175,7 +188,11 @@ __global__ void __launch_bounds__(448, 1)
         const int st = t % NS;
         const int i0 = (qt_first + t) * MQ;
         if (t >= NS) mbar_wait(&q_empty[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
-        mbar_arrive_expect_tx(&q_full[st], 2 * L::kQBytes + 2 * MQ * 4);
+        // the bias stage also held step t-NS's dbias tile until its store read it
+        if (BIAS && p.dbias.data != nullptr && t >= NS)
+          mbar_wait(&dbias_read[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
+        mbar_arrive_expect_tx(&q_full[st],
+                              2 * L::kQBytes + 2 * MQ * 4 + (BIAS ? L::kBiasBytes : 0));
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           tma_load_4d(smem + L::kQ + st * L::kQBytes + s * L::kQSlab, &tm_q, &q_full[st], s * 64,
@@ -186,6 +203,9 @@ __global__ void __launch_bounds__(448, 1)
         const size_t vec = static_cast<size_t>(bh) * p.Sq_pad + i0;
         bulk_load(smem + L::kLse + st * MQ * 4, p.lse2 + vec, MQ * 4, &q_full[st]);
         bulk_load(smem + L::kDelta + st * MQ * 4, p.delta + vec, MQ * 4, &q_full[st]);
+        if (BIAS)  // rows past Sq and keys past Sk read as zeros
+          tma_load_4d(smem + L::kBiasT + st * L::kBiasBytes, &tm_bias, &q_full[st], k0, i0,
+                      p.bias.sH == 0 ? 0 : h, p.bias.sB == 0 ? 0 : b);
       }
       if (*abort_word) {
         for (int t = max(0, n_steps - NS); t < n_steps; ++t)
@@ -294,22 +314,9 @@ __global__ void __launch_bounds__(448, 1)
       const int i0 = (qt_first + t) * MQ;
       const uint32_t lse_s = sb + L::kLse + st * MQ * 4;
       const uint32_t del_s = sb + L::kDelta + st * MQ * 4;
-      // bias(i0 + c, kj) of this step as bf16 pairs (c even: low half),
-      // fetched before the waits so that its latency is hidden
-      uint32_t bpk[MQ / 2];
-      if (BIAS) {
-        const bool key_ok = kj < Sk;
-        const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0);
-#pragma unroll
-        for (int c2 = 0; c2 < MQ / 2; ++c2) {
-          const int ia = i0 + 2 * c2;
-          const uint32_t lo =
-              (key_ok && ia < Sq) ? __ldg(bp + static_cast<int64_t>(ia) * p.bias.sS) : 0u;
-          const uint32_t hi =
-              (key_ok && ia + 1 < Sq) ? __ldg(bp + static_cast<int64_t>(ia + 1) * p.bias.sS) : 0u;
-          bpk[c2] = lo | (hi << 16);
-        }
-      }
+      // this step's bias tile [MQ query rows x 128 keys] (bf16, row-major),
+      // loaded with Q and dO: column r is this thread's key
+      const uint32_t bias_s = sb + L::kBiasT + st * L::kBiasBytes + 2 * r;
       mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
       mbar_wait(&s_full[x], k & 1, wc, kSiteBwdSFull);
       tc_fence_after();
@@ -331,9 +338,7 @@ __global__ void __launch_bounds__(448, 1)
 #pragma unroll
       for (int c = 0; c < MQ; ++c) {
         float arg = fmaf(pv[c], p.scale_log2, -ld_shared_f32(lse_s + c * 4));
-        if (BIAS)
-          arg = fmaf(bf16_bits_to_float((c & 1) ? (bpk[c >> 1] >> 16) : (bpk[c >> 1] & 0xffffu)),
-                     kLog2e, arg);
+        if (BIAS) arg = fmaf(bf16_bits_to_float(ld_shared_u16(bias_s + c * 256)), kLog2e, arg);
         float e = ex2_approx(arg);
         if (need_mask && c < first_vis) e = 0.f;
         pv[c] = e;
@@ -385,16 +390,12 @@ __global__ void __launch_bounds__(448, 1)
           if (DROPOUT) g = ((kb[cc] >> i) & 1u) ? g * p.drop_rescale : 0.f;
           ds[i] = pv[e] * (g - ld_shared_f32(del_s + e * 4));
         }
-        if (BIAS && p.dbias.data != nullptr && kj < Sk) {
-          // dbias(i, kj) = dS(i, kj); a warp writes 64 contiguous bytes per row
-          uint16_t* dp = p.dbias.data + b * p.dbias.sB + h * p.dbias.sH + kj;
+        if (BIAS && p.dbias.data != nullptr) {
+          // dbias(i, kj) = dS(i, kj) replaces this thread's own bias column of
+          // the stage tile (read above); the tile is stored by TMA below
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int qi = i0 + cc * 32 + i;
-            if (qi < Sq)
-              dp[static_cast<int64_t>(qi) * p.dbias.sS] =
-                  static_cast<uint16_t>(pack_bf16x2(ds[i], 0.f) & 0xffffu);
-          }
+          for (int i = 0; i < 32; ++i)
+            st_shared_u16(bias_s + (cc * 32 + i) * 256, pack_bf16x2(ds[i], 0.f) & 0xffffu);
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -409,6 +410,17 @@ __global__ void __launch_bounds__(448, 1)
       mbar_arrive(&sp_empty[x]);
       fence_async_smem();
       mbar_arrive(&ds_full[x]);
+      if (BIAS && p.dbias.data != nullptr) {
+        // the warpgroup's dbias tile [MQ rows x 128 keys]; rows past Sq and
+        // keys past Sk are clipped by the store
+        named_barrier_sync(5 + x, 128);
+        if (r == 0) {
+          tma_store_4d(&tm_dbias, smem + L::kBiasT + st * L::kBiasBytes, k0, i0, h, b);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&dbias_read[st]);
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ dQ warpgroup (warps 8-11)
@@ -520,17 +532,18 @@ __global__ void __launch_bounds__(448, 1)
 template <bool C, bool DR, bool BI, bool VL>
 cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stream) {
   auto kern = bwd_main_kernel_d128<C, DR, BI, VL>;
-  const int smem = B128::kAlloc;
+  const int smem = B128<BI>::kAlloc;
   cudaError_t e = ensure_smem_attr<bwd_main_kernel_d128<C, DR, BI, VL>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
-  kern<<<grid, B128::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], p);
+  kern<<<grid, B128<BI>::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
+                                                   p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t bwd_d128_smem_bytes() { return B128::kAlloc; }
+size_t bwd_d128_smem_bytes() { return B128<false>::kAlloc; }
 
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout, const CUtensorMap* maps,
                                  const BwdParams& p, cudaStream_t stream) {
