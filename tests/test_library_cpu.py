@@ -252,3 +252,33 @@ def test_bias_argument_errors(lib):
     # a gradient needs the bias, and must have the full [B, H, Sq, Sk] shape
     assert bwd(options(dbias=bias())) == 1
     assert bwd(options(attn_bias=bias(Bb=1, Hb=1), dbias=bias(Bb=1))) == 1
+
+
+def test_varlen_argument_errors(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    H, Tq, Tk, D = 2, 300, 400, 64
+    r = ctypes.byref
+    q, kk = desc(1, H, Tq, D, layout="BSHE"), desc(1, H, Tk, D, layout="BSHE")
+
+    def seqs(cq=FAKE, ck=FAKE, batch=3, mq=128, mk=256):
+        v = sdpa.SdpaVarlen()
+        v.cu_seqlens_q, v.cu_seqlens_k = cq, ck
+        v.batch, v.max_seqlen_q, v.max_seqlen_k = batch, mq, mk
+        return v
+
+    def fwd(vl, qq=q, o=None):
+        return lib.sdpa_fwd_varlen(r(qq), r(kk), r(kk), r(vl), 0.0, 1, 0.125, 0, 0, r(qq),
+                                   ctypes.c_void_p(FAKE), o, None)
+
+    assert fwd(seqs(cq=None)) == 1                       # offsets missing
+    assert fwd(seqs(ck=FAKE + 2)) == 3                   # offsets not 4-byte aligned
+    assert fwd(seqs(batch=0)) == 1
+    assert fwd(seqs(mq=0)) == 1
+    assert fwd(seqs(), qq=desc(2, H, Tq, D)) == 1        # packed tensors are [1, H, total, D]
+    keep = desc(1, H, Tq, Tk, stride=(H * Tq * 408, Tq * 408, 408, 1))
+    assert fwd(seqs(), o=r(options(attn_bias=ctypes.addressof(keep)))) == 2  # no bias when packed
+    assert lib.sdpa_bwd_varlen_workspace_size(None, H, D, None) == 0
+    vl = seqs()
+    # workspace as for a [batch, H, max_q] problem
+    assert (lib.sdpa_bwd_varlen_workspace_size(r(vl), H, D, None)
+            == lib.sdpa_bwd_workspace_size(3, H, 128, 256, D))
