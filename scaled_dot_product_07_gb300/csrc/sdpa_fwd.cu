@@ -4,10 +4,13 @@
 // natural-log log-sum-exp of each score row, stashed for the backward
 // (NVIDIA/Fuser issue 2278, "SdpaOpFwd / SdpaOpBwd nodes").
 //
-// One CTA computes two 128-row query tiles (Q0, Q1: 256 rows) of one
-// (batch, head), 320 threads:
-//   warp 9      TMA producer: Q0, Q1 once, then K_j and V_j (separate
-//               barriers) through a ring of 128-byte-swizzled stages.
+// An item is two 128-row query tiles (Q0, Q1: 256 rows) of one (batch,
+// head). Each CTA runs two items back to back (item c and item total-1-c:
+// long causal tile pairs matched with short ones), 320 threads:
+//   warp 9      TMA producer: per item Q0, Q1 (once the previous item's
+//               last S product has read them), then K_j and V_j (separate
+//               barriers) through a ring of 128-byte-swizzled stages that
+//               runs on across items.
 //   warp 8      TMEM allocator and MMA issuer (the warp runs converged, one
 //               elected lane issues the tcgen05 instructions). TMEM holds
 //               S0, S1 (128 fp32 columns each) and O0, O1 (D columns each).
@@ -29,8 +32,10 @@
 //               reference), and stores its half of P (bf16, dropout
 //               applied) into TMEM. Halving the work per thread halves the
 //               softmax latency each tile adds to the ping-pong. At the end
-//               the halves' row sums are combined and out = O / l (TMA store
-//               through shared memory) and lse = m * scale + ln l written.
+//               of an item the halves' row sums are combined and out = O / l
+//               is stored straight from registers (the Q tiles are already
+//               being refilled) and lse = m * scale + ln l written; the next
+//               item's first products run meanwhile.
 // The completion of S_i(j+1) implies that O_i += P_i(j) V_j has completed
 // (tcgen05 operations of one issuing thread complete in order), so the
 // softmax may touch O_i as soon as it sees its next scores.
@@ -53,7 +58,7 @@ struct FwdLayout {
   static constexpr int kRed = kV + kStages * kTileBytes;
   static constexpr int kBar = kRed + 2 * 2 * 2 * 128 * 4;
   // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_full[2]
-  static constexpr int kNumBars = 1 + 4 * kStages + 6;
+  static constexpr int kNumBars = 1 + 4 * kStages + 6 + 1;  // + q_free
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;             // room to align to 1024
@@ -82,11 +87,54 @@ __device__ __forceinline__ int kv_tiles_for(int r0, int Sq, int Sk, bool causal)
   return min(n, min(r0 + 127, Sq - 1) / 128 + 1);
 }
 
+// One unit of work: a pair of 128-row query tiles of one (batch, head).
+struct FwdItem {
+  int b, h, bh, q0, Sq, Sk, qs, ks, tb;
+  int n_t0, n_t1, n_kv;
+  bool active;   // the tile pair holds query rows
+  bool no_keys;  // a packed sequence with queries and no keys
+};
+
+// Head-major item order (a head's K/V stays in L2 while its items run); within
+// a head the longest causal tile pairs come first.
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
+  FwdItem it;
+  const int n_pairs = p.n_q_tiles;
+  const int slot = item / n_pairs;
+  int pair = item - slot * n_pairs;
+  if (CAUSAL) pair = n_pairs - 1 - pair;
+  // batch-major, or head-major when a bias shared by the batch makes the
+  // batches of one head read the same bias tiles
+  it.b = p.h_major ? slot % p.B : slot / p.H;
+  it.h = p.h_major ? slot / p.B : slot - it.b * p.H;
+  it.bh = it.b * p.H + it.h;
+  it.q0 = pair * 256;
+  // the sequence: the whole [Sq, Sk] problem, or sequence b of a packed batch
+  it.Sq = p.Sq;
+  it.Sk = p.Sk;
+  it.qs = 0;
+  it.ks = 0;
+  if (VARLEN) {
+    it.qs = p.cu_q[it.b];
+    it.Sq = p.cu_q[it.b + 1] - it.qs;
+    it.ks = p.cu_k[it.b];
+    it.Sk = p.cu_k[it.b + 1] - it.ks;
+  }
+  it.tb = VARLEN ? 0 : it.b;  // batch coordinate in the tensor maps
+  it.active = it.q0 < it.Sq;
+  it.no_keys = it.active && it.Sk <= 0;
+  const bool work = it.active && !it.no_keys;
+  it.n_t0 = work ? kv_tiles_for(it.q0, it.Sq, it.Sk, CAUSAL) : 0;
+  it.n_t1 = work ? kv_tiles_for(it.q0 + 128, it.Sq, it.Sk, CAUSAL) : 0;
+  it.n_kv = max(it.n_t0, it.n_t1);
+  return it;
+}
+
 template <int D, bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-               const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using L = FwdLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -103,49 +151,26 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* s_full = v_empty + S;    // [2]
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_full = p_full + 2;     // [2]
+  uint64_t* q_free = o_full + 2;     // every S product of an item has read Q0, Q1
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // head-major order (a head's K/V stays in L2 while its tiles run);
-  // within a head the longest causal tiles go first
-  const int n_pairs = p.n_q_tiles;  // tile pairs per head
-  const int slot = blockIdx.x / n_pairs;
-  int pair = blockIdx.x - slot * n_pairs;
-  if (CAUSAL) pair = n_pairs - 1 - pair;
-  // (b, h) of this CTA: batch-major, or head-major when a bias shared by the
-  // batch makes the batches of one head read the same bias tiles
-  const int b = p.h_major ? slot % p.B : slot / p.H;
-  const int h = p.h_major ? slot / p.B : slot - b * p.H;
-  const int bh = b * p.H + h;
-  const int q0 = pair * 256;
-  // the sequence: the whole [Sq, Sk] problem, or sequence b of a packed batch
-  int Sq = p.Sq, Sk = p.Sk, qs = 0, ks = 0;
-  if (VARLEN) {
-    qs = p.cu_q[b];
-    Sq = p.cu_q[b + 1] - qs;
-    ks = p.cu_k[b];
-    Sk = p.cu_k[b + 1] - ks;
-    if (q0 >= Sq) return;  // the sequence has no query rows in this tile pair
-    if (Sk <= 0) {
-      // no keys: the rows' outputs are 0 and their log-sum-exp is -inf
-      for (int r = threadIdx.x; r < 256 && q0 + r < Sq; r += blockDim.x) {
-        uint16_t* o = static_cast<uint16_t*>(p.out_io.data) + h * p.out_io.sH +
-                      static_cast<int64_t>(qs + q0 + r) * p.out_io.sS;
-        for (int c = 0; c < p.D_io; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
-        p.lse[static_cast<size_t>(h) * p.total_q + qs + q0 + r] = -INFINITY;
-      }
-      return;
-    }
-  }
-  const int tb = VARLEN ? 0 : b;  // batch coordinate in the tensor maps
-  const int n_t[2] = {kv_tiles_for(q0, Sq, Sk, CAUSAL), kv_tiles_for(q0 + 128, Sq, Sk, CAUSAL)};
-  const int n_kv = max(n_t[0], n_t[1]);
+  // CTA c runs item c and then item total-1-c: in the head-major order the
+  // long causal tile pairs of one window are matched with the short ones of
+  // the other, so every CTA gets about the same work, and the second item's
+  // Q and first K/V tiles load while the first item finishes.
+  const int total = p.n_q_tiles * p.B * p.H;
+  const int first_item = blockIdx.x;
+  const int second_item = total - 1 - static_cast<int>(blockIdx.x);
+  const int n_items = second_item > first_item ? 2 : 1;
+  auto item_id = [&](int k) { return k == 0 ? first_item : second_item; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_free, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -176,36 +201,45 @@ __global__ void __launch_bounds__(320, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const int nq = n_t[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
-      for (int i = 0; i < nq; ++i) {
+      int qk = 0;  // Q loads issued (phases of q_full / q_free)
+      int g = 0;   // K / V tiles issued over all items (ring position)
+      for (int k = 0; k < n_items; ++k) {
+        const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, item_id(k));
+        if (it.n_kv == 0) continue;
+        // Q0, Q1 of the previous item are free once its last S product is done
+        if (qk >= 1) mbar_wait(q_free, (qk - 1) & 1, wc, kSiteFwdQFull);
+        const int nq = it.n_t1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+        for (int i = 0; i < nq; ++i) {
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, &tm_q, q_full, s * 64,
-                      qs + q0 + 128 * i, h, tb);
-      }
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % S;
-        // a K stage is free once the last S MMA reading it is done, a V stage
-        // once the last P V MMA reading it is done
-        if (j >= S) mbar_wait(&k_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
-        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, &tm_q, q_full,
+                        s * 64, it.qs + it.q0 + 128 * i, it.h, it.tb);
+        }
+        ++qk;
+        for (int j = 0; j < it.n_kv; ++j, ++g) {
+          const int st = g % S;
+          // a K stage is free once the last S MMA reading it is done, a V stage
+          // once the last P V MMA reading it is done
+          if (g >= S) mbar_wait(&k_empty[st], ((g / S) - 1) & 1, wc, kSiteFwdKvEmpty);
+          mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
-                      s * 64, ks + j * 128, h, tb);
-        if (j >= S) mbar_wait(&v_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
-        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
+                        s * 64, it.ks + j * 128, it.h, it.tb);
+          if (g >= S) mbar_wait(&v_empty[st], ((g / S) - 1) & 1, wc, kSiteFwdKvEmpty);
+          mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &v_full[st],
-                      s * 64, ks + j * 128, h, tb);
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &v_full[st],
+                        s * 64, it.ks + j * 128, it.h, it.tb);
+        }
       }
       if (*abort_word) {
         // give the loads still in flight time to land before the CTA exits
-        for (int j = max(0, n_kv - S); j < n_kv; ++j) {
-          mbar_wait_drain(&k_full[j % S], (j / S) & 1, 2000000ull);
-          mbar_wait_drain(&v_full[j % S], (j / S) & 1, 2000000ull);
+        for (int gg = max(0, g - S); gg < g; ++gg) {
+          mbar_wait_drain(&k_full[gg % S], (gg / S) & 1, 2000000ull);
+          mbar_wait_drain(&v_full[gg % S], (gg / S) & 1, 2000000ull);
         }
       }
     }
@@ -214,11 +248,12 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (waits and descriptor arithmetic are
     // warp-uniform); one elected lane issues the tcgen05 instructions.
+    // Per key tile j it issues O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j,
+    // S1 = Q1 K_{j+1}^T (ping-pong between the two query tiles).
     const uint32_t leader = elect_one();
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-    auto issue_s = [&](int i, int j) {
-      const int st = j % S;
+    auto issue_s = [&](int i, int st) {
       const uint64_t qd = sdesc_sw128(sb + L::kQ + i * L::kTileBytes, 16, 1024);
       const uint64_t kd = sdesc_sw128(sb + L::kK + st * L::kTileBytes, 16, 1024);
 #pragma unroll
@@ -229,41 +264,54 @@ __global__ void __launch_bounds__(320, 1)
       }
       mma_commit_if(leader, &s_full[i]);
     };
-    auto issue_pv = [&](int i, int j) {
-      const int st = j % S;
+    auto issue_pv = [&](int i, int st, bool first) {
       const uint64_t vd = sdesc_sw128(sb + L::kV + st * L::kTileBytes, L::kSlabBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_bf16_ts_if(leader, tmem + L::tmem_o(i), tmem + L::tmem_s(i) + kk * 8,
-                       sdesc_add(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+                       sdesc_add(vd, kk * 2048), kIdO, (!first || kk > 0) ? 1u : 0u);
     };
-    mbar_wait(q_full, 0, wc, kSiteFwdQFull);
-    if (n_kv > 0) {
-      mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+    int qk = 0, g = 0;
+    int pc[2] = {0, 0};  // P tiles consumed per query tile (phases of p_full)
+    for (int k = 0; k < n_items; ++k) {
+      const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, item_id(k));
+      if (it.n_kv == 0) continue;
+      const int n_t[2] = {it.n_t0, it.n_t1};
+      mbar_wait(q_full, qk & 1, wc, kSiteFwdQFull);
+      ++qk;
+      const int g0 = g;
+      mbar_wait(&k_full[g0 % S], (g0 / S) & 1, wc, kSiteFwdKvFull);
       tc_fence_after();
       for (int i = 0; i < 2; ++i)
-        if (n_t[i] > 0) issue_s(i, 0);
-      mma_commit_if(leader, &k_empty[0]);  // K_0 has no other reader
-    }
-    for (int j = 0; j < n_kv; ++j) {
-      const int st = j % S;
-      mbar_wait(&v_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
-      for (int i = 0; i < 2; ++i) {
-        if (j >= n_t[i]) continue;
-        mbar_wait(&p_full[i], j & 1, wc, kSiteFwdPFull);
-        tc_fence_after();
-        issue_pv(i, j);
-        if (j + 1 < n_t[i]) {
-          const int st1 = (j + 1) % S;
-          mbar_wait(&k_full[st1], ((j + 1) / S) & 1, wc, kSiteFwdKvFull);
+        if (n_t[i] > 0) issue_s(i, g0 % S);
+      mma_commit_if(leader, &k_empty[g0 % S]);  // K_0 has no other reader
+      if (it.n_kv == 1) mma_commit_if(leader, q_free);
+      for (int j = 0; j < it.n_kv; ++j) {
+        const int gj = g0 + j;
+        const int st = gj % S;
+        mbar_wait(&v_full[st], (gj / S) & 1, wc, kSiteFwdKvFull);
+        for (int i = 0; i < 2; ++i) {
+          if (j >= n_t[i]) continue;
+          // P_i of this tile; it also orders the previous item's epilogue
+          // reads of O_i before the first P V product overwrites O_i
+          mbar_wait(&p_full[i], pc[i] & 1, wc, kSiteFwdPFull);
+          ++pc[i];
           tc_fence_after();
-          issue_s(i, j + 1);
-        } else {
-          mma_commit_if(leader, &o_full[i]);
+          issue_pv(i, st, j == 0);
+          if (j + 1 < n_t[i]) {
+            const int g1 = gj + 1;
+            mbar_wait(&k_full[g1 % S], (g1 / S) & 1, wc, kSiteFwdKvFull);
+            tc_fence_after();
+            issue_s(i, g1 % S);
+          } else {
+            mma_commit_if(leader, &o_full[i]);
+          }
         }
+        mma_commit_if(leader, &v_empty[st]);                                 // V_j read by both P V
+        if (j + 1 < it.n_kv) mma_commit_if(leader, &k_empty[(gj + 1) % S]);  // K_{j+1} by both S
+        if (j + 2 == it.n_kv) mma_commit_if(leader, q_free);  // the item's last S is issued
       }
-      mma_commit_if(leader, &v_empty[st]);                             // V_j read by both P V
-      if (j + 1 < n_kv) mma_commit_if(leader, &k_empty[(j + 1) % S]);  // K_{j+1} by both S
+      g += it.n_kv;
     }
     __syncwarp();
   } else {
@@ -280,208 +328,207 @@ __global__ void __launch_bounds__(320, 1)
     float* red = reinterpret_cast<float*>(smem + L::kRed);
     const float sl2 = p.scale_log2;
     const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
-    float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
-    float l[2] = {0.f, 0.f};              // this half's running sum, per tile
-    // the half's tile max, shared with the partner half; returns the row's tile max
-    auto exchange_max = [&](int i, int j, float mh) {
-      float* slot = red + ((i * 2 + (j & 1)) * 2) * 128;
-      slot[half * 128 + row] = mh;
+    int sc[2] = {0, 0};  // S tiles consumed per query tile (phases of s_full)
+    int oc[2] = {0, 0};  // items finished per query tile (phases of o_full)
+    int xc[2] = {0, 0};  // exchanges per query tile; consecutive ones use alternate slots
+    // this half's value v, shared with the partner half through the tile's
+    // next exchange slot; returns the partner's value
+    auto exchange = [&](int i, float v) {
+      float* slot = red + ((i * 2 + (xc[i] & 1)) * 2) * 128;
+      ++xc[i];
+      slot[half * 128 + row] = v;
       // also orders the partner's TMEM score reads before this warp's P
       // stores into the same columns
       tc_fence_before();
       named_barrier_sync(pair_bar + 4 * i, 64);
       tc_fence_after();
-      return fmaxf(mh, slot[(1 - half) * 128 + row]);
+      return slot[(1 - half) * 128 + row];
     };
 
-    for (int j = 0; j < n_kv; ++j) {
-      for (int i = 0; i < 2; ++i) {
-        if (j >= n_t[i]) continue;
-        const int qi = q0 + 128 * i + row;
-        const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
-        const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-        // the half row's 64 bias values, fetched before the scores are ready
-        uint4 bv[8];
-        if (BIAS) {
-          // start the next key tile's bias line towards L2
-          const int kn = (j + 1) * 128 + 64 * half;
-          if (j + 1 < n_t[i] && kn < Sk) {
-            const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
-            prefetch_l2(np);
-            prefetch_l2(np + min(56, Sk - 1 - kn));
-          }
-          const int kb = j * 128 + 64 * half;
-          const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                               static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            if (kb + 8 * c + 8 <= Sk) {
-              bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
-            } else {
-              // key tail: only the keys that exist are read
-              uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (kb + 8 * c + e < Sk)
-                  w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
-              bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int k = 0; k < n_items; ++k) {
+      const FwdItem it = fwd_item<CAUSAL, VARLEN>(p, item_id(k));
+      if (!it.active) continue;
+      const int b = it.b, h = it.h, bh = it.bh, q0 = it.q0, Sq = it.Sq, Sk = it.Sk, qs = it.qs;
+      if (it.no_keys) {
+        // no keys: the rows' outputs are 0 and their log-sum-exp is -inf
+        for (int r = threadIdx.x; r < 256 && q0 + r < Sq; r += 256) {
+          uint16_t* o = static_cast<uint16_t*>(p.out_io.data) + h * p.out_io.sH +
+                        static_cast<int64_t>(qs + q0 + r) * p.out_io.sS;
+          for (int c = 0; c < p.D_io; c += 8)
+            *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+          p.lse[static_cast<size_t>(h) * p.total_q + qs + q0 + r] = -INFINITY;
+        }
+        continue;
+      }
+      const int n_t[2] = {it.n_t0, it.n_t1};
+      float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
+      float l[2] = {0.f, 0.f};              // this half's running sum, per tile
+      for (int j = 0; j < it.n_kv; ++j) {
+        for (int i = 0; i < 2; ++i) {
+          if (j >= n_t[i]) continue;
+          const int qi = q0 + 128 * i + row;
+          const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
+          const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+          // the half row's 64 bias values, fetched before the scores are ready
+          uint4 bv[8];
+          if (BIAS) {
+            // start the next key tile's bias line towards L2
+            const int kn = (j + 1) * 128 + 64 * half;
+            if (j + 1 < n_t[i] && kn < Sk) {
+              const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                                   static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
+              prefetch_l2(np);
+              prefetch_l2(np + min(56, Sk - 1 - kn));
+            }
+            const int kb = j * 128 + 64 * half;
+            const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
+  #pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              if (kb + 8 * c + 8 <= Sk) {
+                bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
+              } else {
+                // key tail: only the keys that exist are read
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+  #pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (kb + 8 * c + e < Sk)
+                    w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
+                bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
+              }
             }
           }
-        }
-        mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tS + 64 * half, r0);
-        tmem_ld32(tS + 64 * half + 32, r1);
-        tmem_ld_wait(r0);
-        reg_touch(r1);
-        float x[64];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] = __uint_as_float(r0[c]);
-          x[32 + c] = __uint_as_float(r1[c]);
-        }
-        if (BIAS) {
-          // the bias in raw-score units (scores are scaled at the exponential)
-          const float inv = p.bias_to_raw;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t w[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              x[8 * c + 2 * e] = fmaf(bf16_bits_to_float(w[e] & 0xffffu), inv, x[8 * c + 2 * e]);
-              x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
+          mbar_wait(&s_full[i], sc[i] & 1, wc, kSiteFwdSFull);
+          ++sc[i];
+          tc_fence_after();
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tS + 64 * half, r0);
+          tmem_ld32(tS + 64 * half + 32, r1);
+          tmem_ld_wait(r0);
+          reg_touch(r1);
+          float x[64];
+  #pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            x[c] = __uint_as_float(r0[c]);
+            x[32 + c] = __uint_as_float(r1[c]);
+          }
+          if (BIAS) {
+            // the bias in raw-score units (scores are scaled at the exponential)
+            const float inv = p.bias_to_raw;
+  #pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t w[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[8 * c + 2 * e] = fmaf(bf16_bits_to_float(w[e] & 0xffffu), inv, x[8 * c + 2 * e]);
+                x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
+              }
             }
           }
-        }
-        const int k0 = j * 128 + 64 * half;  // first key of this half
-        if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
-          const int lim = CAUSAL ? min(Sk - k0, qi - k0 + 1) : (Sk - k0);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c >= lim) x[c] = -INFINITY;
-        }
-        // half-row max as 8 independent chains, then combined
-        float mp[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
-#pragma unroll
-        for (int c = 16; c < 64; c += 16)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
-        const float mh =
-            fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
-        const float m_new = fmaxf(m[i], exchange_max(i, j, mh));
-        if (j == 0) {
-          m[i] = m_new;
-        } else if (__any_sync(0xffffffffu, (m_new - m[i]) * sl2 > 8.0f)) {
-          // both halves of these rows take this branch (same rows, same maxima);
-          // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
-          const float alpha = ex2_approx((m[i] - m_new) * sl2);
-          l[i] *= alpha;
-          m[i] = m_new;
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
-            uint32_t o[32];
-            tmem_ld32(tO + (D / 2) * half + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + (D / 2) * half + c * 32, o);
+          const int k0 = j * 128 + 64 * half;  // first key of this half
+          if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
+            const int lim = CAUSAL ? min(Sk - k0, qi - k0 + 1) : (Sk - k0);
+  #pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c >= lim) x[c] = -INFINITY;
           }
-        }
-        const float neg = -m[i] * sl2;
+          // half-row max as 8 independent chains, then combined
+          float mp[8];
+  #pragma unroll
+          for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
+  #pragma unroll
+          for (int c = 16; c < 64; c += 16)
+  #pragma unroll
+            for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
+          const float mh =
+              fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
+          const float m_new = fmaxf(m[i], fmaxf(mh, exchange(i, mh)));
+          if (j == 0) {
+            m[i] = m_new;
+          } else if (__any_sync(0xffffffffu, (m_new - m[i]) * sl2 > 8.0f)) {
+            // both halves of these rows take this branch (same rows, same maxima);
+            // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
+            const float alpha = ex2_approx((m[i] - m_new) * sl2);
+            l[i] *= alpha;
+            m[i] = m_new;
+  #pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
+              uint32_t o[32];
+              tmem_ld32(tO + (D / 2) * half + c * 32, o);
+              tmem_ld_wait(o);
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(tO + (D / 2) * half + c * 32, o);
+            }
+          }
+          const float neg = -m[i] * sl2;
 
-        uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
-        if (DROPOUT) {
-          const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + qi) *
-                                 static_cast<uint64_t>(p.Sk_ctr);
-          keep_bits<2>(n_row + k0, p.drop_threshold, pk, keep);
-        }
-        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
-        uint32_t pk2[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float e0 = ex2_approx(fmaf(x[c], sl2, neg));
-          float e1 = ex2_approx(fmaf(x[c + 1], sl2, neg));
-          rs[(c >> 1) & 7] += e0 + e1;
+          uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
           if (DROPOUT) {
-            e0 = ((keep[c >> 5] >> (c & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
-            e1 = ((keep[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
+            const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + qi) *
+                                   static_cast<uint64_t>(p.Sk_ctr);
+            keep_bits<2>(n_row + k0, p.drop_threshold, pk, keep);
           }
-          pk2[c >> 1] = pack_bf16x2(e0, e1);
+          float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
+          uint32_t pk2[32];
+  #pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            float e0 = ex2_approx(fmaf(x[c], sl2, neg));
+            float e1 = ex2_approx(fmaf(x[c + 1], sl2, neg));
+            rs[(c >> 1) & 7] += e0 + e1;
+            if (DROPOUT) {
+              e0 = ((keep[c >> 5] >> (c & 31)) & 1u) ? e0 * p.drop_rescale : 0.f;
+              e1 = ((keep[(c + 1) >> 5] >> ((c + 1) & 31)) & 1u) ? e1 * p.drop_rescale : 0.f;
+            }
+            pk2[c >> 1] = pack_bf16x2(e0, e1);
+          }
+          // P (bf16 pairs) of keys [64h, 64h+64) -> S columns [32h, 32h+32); they
+          // overwrite scores this warp pair has already read
+          tmem_st32(tS + 32 * half, pk2);
+          l[i] += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_full[i]);
         }
-        // P (bf16 pairs) of keys [64h, 64h+64) -> S columns [32h, 32h+32); they
-        // overwrite scores this warp pair has already read
-        tmem_st32(tS + 32 * half, pk2);
-        l[i] += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_full[i]);
       }
-    }
-
-    // ------------------------------------------------------------ epilogue
-    for (int i = 0; i < 2; ++i) {
-      if (n_t[i] == 0) continue;
-      const int qi = q0 + 128 * i + row;
-      const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-      // the row sum is the sum of both halves (slot parity n_t[i] is unused by
-      // the last tile's max exchange)
-      const float l_row = [&] {
-        float* slot = red + ((i * 2 + (n_t[i] & 1)) * 2) * 128;
-        slot[half * 128 + row] = l[i];
-        named_barrier_sync(pair_bar + 4 * i, 64);
-        return l[i] + slot[(1 - half) * 128 + row];
-      }();
-      mbar_wait(&o_full[i], 0, wc, kSiteFwdODone);
-      tc_fence_after();
-      const float inv_l = 1.f / l_row;
-      const uint32_t oa = sb + L::kQ + i * L::kTileBytes;  // Q_i is dead after o_full[i]
-      // a packed sequence's last tile is stored row by row, so that rows of
-      // the next sequence are never written (uniform over the CTA)
-      const bool direct = VARLEN && (q0 + 128 * i + 128 > Sq);
+      // ---------------------------------------------------------- epilogue
+      for (int i = 0; i < 2; ++i) {
+        if (n_t[i] == 0) continue;
+        const int qi = q0 + 128 * i + row;
+        const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+        // the row sum is the sum of both halves
+        const float l_row = l[i] + exchange(i, l[i]);
+        mbar_wait(&o_full[i], oc[i] & 1, wc, kSiteFwdODone);
+        ++oc[i];
+        tc_fence_after();
+        const float inv_l = 1.f / l_row;
+        // rows are stored straight from registers (the Q tiles are being
+        // refilled for the next item); columns past D_io are padding
+        uint16_t* orow = static_cast<uint16_t*>(p.out_io.data) + it.tb * p.out_io.sB +
+                         h * p.out_io.sH + static_cast<int64_t>(qs + qi) * p.out_io.sS;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns
-        uint32_t o[32];
-        tmem_ld32(tO + (D / 2) * half + c * 32, o);
-        tmem_ld_wait(o);
+        for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns
+          uint32_t o[32];
+          tmem_ld32(tO + (D / 2) * half + c * 32, o);
+          tmem_ld_wait(o);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int col0 = (D / 2) * half + c * 32 + q4 * 8;
-          const uint32_t w0 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
-                                          __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-          const uint32_t w1 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
-                                          __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-          const uint32_t w2 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
-                                          __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-          const uint32_t w3 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
-                                          __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-          if (direct) {
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int col0 = (D / 2) * half + c * 32 + q4 * 8;
+            const uint32_t w0 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
+                                            __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+            const uint32_t w1 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
+                                            __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+            const uint32_t w2 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
+                                            __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+            const uint32_t w3 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
+                                            __uint_as_float(o[q4 * 8 + 7]) * inv_l);
             if (qi < Sq && col0 < p.D_io)
-              *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out_io.data) + h * p.out_io.sH +
-                                        static_cast<int64_t>(qs + qi) * p.out_io.sS + col0) =
-                  make_uint4(w0, w1, w2, w3);
-          } else {
-            st_shared_v4(oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3),
-                         w0, w1, w2, w3);
+              *reinterpret_cast<uint4*>(orow + col0) = make_uint4(w0, w1, w2, w3);
           }
         }
-      }
-      if (half == 0 && qi < Sq)
-        p.lse[(VARLEN ? static_cast<size_t>(h) * p.total_q + qs : static_cast<size_t>(bh) * Sq) +
-              qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
-      if (direct) continue;
-      fence_async_smem();
-      named_barrier_sync(9 + i, 256);
-      if (threadIdx.x == 0) {
-#pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_store_4d(&tm_o, smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, s * 64,
-                       qs + q0 + 128 * i, h, tb);
-        bulk_commit();
-        bulk_wait_all();
+        if (half == 0 && qi < Sq)
+          p.lse[(VARLEN ? static_cast<size_t>(h) * p.total_q + qs : static_cast<size_t>(bh) * Sq) +
+                qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
       }
     }
   }
@@ -500,8 +547,10 @@ cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream
   const int smem = FwdLayout<D>::kAlloc;
   cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, BI, VL>>(smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
-  kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  // two items (query-tile pairs) per CTA
+  const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
+  const unsigned grid = (items + 1) / 2;
+  kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
   return cudaGetLastError();
 }
 
