@@ -19,8 +19,9 @@ roofline    the backward (dominant) and forward kernels against the measured
 extended    the options entry points on the same workload: the step recorded
             once as a CUDA graph (rng state read from device memory) and
             replayed, and the deterministic (fixed-order dQ) backward; the
-            same shape at head dim 96; with an additive relative-position
-            bias (and its gradient); and a packed batch of mixed lengths.
+            same shape with dropout 0.1; at head dim 96; with an additive
+            relative-position bias (and its gradient); and a packed batch of
+            mixed lengths.
 cpu_baseline / --impl reference: the fp64 CPU oracle on a bounded sample of
             the same workload (whole heads), on this host's cores.
 """
@@ -369,6 +370,18 @@ def bench_ours(args, w):
             "ms": d_ms, "tflops": f_bwd / (d_ms * 1e-3) / 1e12, "workspace_bytes": ws_det.numel(),
             "note": "one fp32 dQ partial per 128-key tile, summed in key-tile order"}
         del ws_det
+        # dropout on the same shape: the keep mask is drawn inside the kernels
+        # (Philox4x32-10 on the absolute element index), forward and backward
+        p_d = 0.1
+        fwd_d = timed(lambda: sdpa.sdpa_fwd(q, k, v, p_d, w.is_causal, None, w.seed, w.offset,
+                                            out=out, lse=lse), 5)
+        bwd_d = timed(lambda: sdpa.sdpa_bwd(do, q, k, v, out, lse, p_d, w.is_causal, w.seed,
+                                            w.offset, None, dq=dq, dk=dk, dv=dv, workspace=ws), 5)
+        extras["dropout_0.1"] = {
+            "fwd_ms": fwd_d, "fwd_tflops": f_fwd / (fwd_d * 1e-3) / 1e12,
+            "bwd_ms": bwd_d, "bwd_tflops": f_bwd / (bwd_d * 1e-3) / 1e12,
+            "note": "dropout_p 0.1 on the same B, H, S, D; the mask is regenerated in the "
+                    "backward"}
         # a head dim the kernels are not built for (96: the 128-wide kernels
         # with the last 32 columns zero-filled by TMA), same B, H, S
         w96 = W.Workload(w.name + "_d96", w.B, w.H, w.Sq, w.Sk, 96, w.is_causal, w.dropout_p,
@@ -564,11 +577,18 @@ def main():
                     help="skip the CUDA-graph and deterministic-backward timings")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (small cases for profiling; not a bench line)")
+    ap.add_argument("--dropout", type=float, default=None,
+                    help="override dropout_p (profiling the dropout path; not a bench line)")
     args = ap.parse_args()
     from scaled_dot_product_07_gb300 import workloads as W
     w = W.WORKLOADS[WORKLOAD]
+    over = {}
     if args.batch is not None:
-        w = W.make_workload(WORKLOAD, B=args.batch)
+        over["B"] = args.batch
+    if args.dropout is not None:
+        over["dropout_p"] = args.dropout
+    if over:
+        w = W.make_workload(WORKLOAD, **over)
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_ours(args, w)

@@ -29,16 +29,15 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
                                                uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo_a = 0xD2511F53u * c0;
-    const uint32_t hi_a = __umulhi(0xD2511F53u, c0);
-    const uint32_t lo_b = 0xCD9E8D57u * c2;
-    const uint32_t hi_b = __umulhi(0xCD9E8D57u, c2);
-    const uint32_t n0 = hi_b ^ c1 ^ k0;
-    const uint32_t n2 = hi_a ^ c3 ^ k1;
+    // one 32x32 -> 64-bit product gives both halves
+    const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ c1 ^ k0;
+    const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ c3 ^ k1;
     c0 = n0;
-    c1 = lo_b;
+    c1 = static_cast<uint32_t>(pb);
     c2 = n2;
-    c3 = lo_a;
+    c3 = static_cast<uint32_t>(pa);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -72,6 +71,44 @@ __device__ __forceinline__ void keep_bits(uint64_t n0, uint32_t threshold, const
   }
 #pragma unroll
   for (int i = 0; i < W; ++i) bits[i] = __funnelshift_r(s[i], s[i + 1], a);
+}
+
+// Keep bits of one key column: the 32*W elements (i0 + c, kj), c < 32W, whose
+// absolute indices are n_base + c*Sk (n_base the index of (i0, kj)). For Sk a
+// multiple of 4 the four lanes of a quad (lanes 4m .. 4m+3 of a warp, holding
+// keys 4u .. 4u+3 in that order, all with the same i0) need the same groups:
+// group (n_base + c*Sk) >> 2 holds the quad's four keys at row i0 + c. Lane
+// q = lane & 3 draws the groups of rows c = 4t + q and the quad swaps the
+// keep nibbles, so each group is drawn once instead of four times. Bit c of
+// kb[c / 32] is 1 iff element (i0 + c, kj) is kept. All 32 lanes of the warp
+// must call it together.
+template <int W>
+__device__ __forceinline__ void keep_bits_quad(uint64_t n_base, uint64_t Sk, uint32_t threshold,
+                                               const PhiloxKey& pk, uint32_t (&kb)[W]) {
+  const uint32_t q = threadIdx.x & 3u;
+  const uint32_t quad = threadIdx.x & 28u;  // lane of the quad's first key
+  const uint64_t g0 = n_base >> 2;
+  const uint64_t gs = Sk >> 2;
+#pragma unroll
+  for (int m = 0; m < W; ++m) {
+    // nibble t: keep bits of the quad's keys 0..3 at row 32m + 4t + q
+    uint32_t own = 0u;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint4 u = philox_group(g0 + static_cast<uint64_t>(32 * m + 4 * t + q) * gs, pk);
+      const uint32_t nib = (u.x >= threshold ? 1u : 0u) | (u.y >= threshold ? 2u : 0u) |
+                           (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
+      own |= nib << (4 * t);
+    }
+    // row 32m + 4t + o comes from lane o of the quad, bit q of its nibble t
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      const uint32_t wo = __shfl_sync(0xffffffffu, own, quad | static_cast<uint32_t>(o));
+      bits |= ((wo >> q) & 0x11111111u) << o;
+    }
+    kb[m] = bits;
+  }
 }
 
 // The key of one launch: the one passed in the kernel parameters, or, when

@@ -489,6 +489,27 @@ __global__ void __launch_bounds__(320, 1)
       const bool key_ok = kj < Sk;
       const uint16_t* bp = BIAS ? p.bias.data + b * p.bias.sB + h * p.bias.sH + (key_ok ? kj : 0)
                                 : nullptr;
+      // the step's dropout keep bits depend only on the indices: drawn while
+      // the tensor core computes S^T
+      uint32_t kb[MQ / 32];
+#pragma unroll
+      for (int w = 0; w < MQ / 32; ++w) kb[w] = 0xffffffffu;
+      if (DROPOUT) {
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
+                                    static_cast<uint64_t>(p.Sk_ctr) +
+                                kj;
+        if ((p.Sk_ctr & 3) == 0) {
+          keep_bits_quad<MQ / 32>(n_base, static_cast<uint64_t>(p.Sk_ctr), p.drop_threshold, pk,
+                                  kb);
+        } else {
+#pragma unroll
+          for (int c = 0; c < MQ; ++c) {
+            const bool kp =
+                keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
+            if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
+          }
+        }
+      }
       mbar_wait(&q_full[st], (t / S) & 1, wc, kSiteBwdQFull);
       mbar_wait(s_full, t & 1, wc, kSiteBwdSFull);
       tc_fence_after();
@@ -522,19 +543,6 @@ __global__ void __launch_bounds__(320, 1)
           float e = ex2_approx(arg);
           if (need_mask && c < first_vis) e = 0.f;
           pv[c] = e;
-        }
-      }
-      uint32_t kb[MQ / 32];
-#pragma unroll
-      for (int w = 0; w < MQ / 32; ++w) kb[w] = 0xffffffffu;
-      if (DROPOUT) {
-        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
-                                    static_cast<uint64_t>(p.Sk_ctr) +
-                                kj;
-#pragma unroll
-        for (int c = 0; c < MQ; ++c) {
-          const bool kp = keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
-          if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
         }
       }
       if (t >= 1) mbar_wait(pds_empty, (t - 1) & 1, wc, kSiteBwdPdsEmpty);

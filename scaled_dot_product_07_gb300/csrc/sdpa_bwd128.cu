@@ -317,6 +317,24 @@ __global__ void __launch_bounds__(448, 1)
       // this step's bias tile [MQ query rows x 128 keys] (bf16, row-major),
       // loaded with Q and dO: column r is this thread's key
       const uint32_t bias_s = sb + L::kBiasT + st * L::kBiasBytes + 2 * r;
+      // the step's dropout keep bits depend only on the indices: drawn while
+      // the tensor core computes S^T
+      uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
+      if (DROPOUT) {
+        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
+                                    static_cast<uint64_t>(p.Sk_ctr) +
+                                kj;
+        if ((p.Sk_ctr & 3) == 0) {
+          keep_bits_quad<2>(n_base, static_cast<uint64_t>(p.Sk_ctr), p.drop_threshold, pk, kb);
+        } else {
+#pragma unroll
+          for (int c = 0; c < MQ; ++c) {
+            const bool kp =
+                keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
+            if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
+          }
+        }
+      }
       mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
       mbar_wait(&s_full[x], k & 1, wc, kSiteBwdSFull);
       tc_fence_after();
@@ -342,18 +360,6 @@ __global__ void __launch_bounds__(448, 1)
         float e = ex2_approx(arg);
         if (need_mask && c < first_vis) e = 0.f;
         pv[c] = e;
-      }
-      uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
-      if (DROPOUT) {
-        const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
-                                    static_cast<uint64_t>(p.Sk_ctr) +
-                                kj;
-#pragma unroll
-        for (int c = 0; c < MQ; ++c) {
-          const bool kp =
-              keep_one(n_base + static_cast<uint64_t>(c) * p.Sk_ctr, p.drop_threshold, pk);
-          if (!kp) kb[c >> 5] &= ~(1u << (c & 31));
-        }
       }
       {
         // P~^T (bf16) into this step's S^T columns [0, 32) of TMEM

@@ -155,7 +155,10 @@ def _block_select_inputs(Sq, Sk, D, j0, i0):
     return tuple(x.to(torch.bfloat16) for x in (q, k, v, do))
 
 
-@pytest.mark.parametrize("D,Sq,Sk,j0,i0", [(64, 256, 300, 100, 150), (128, 300, 520, 260, 40)])
+# key counts that are multiples of 4 take the backward's quad-shared mask
+# draws, the others its per-element draws
+@pytest.mark.parametrize("D,Sq,Sk,j0,i0", [(64, 256, 300, 100, 150), (128, 300, 520, 260, 40),
+                                           (64, 256, 301, 98, 150), (128, 300, 523, 262, 40)])
 def test_kernel_masks_match_oracle_bit_exact(cuda_lib, D, Sq, Sk, j0, i0):
     """The forward and backward kernels drop exactly the oracle's elements.
 
