@@ -56,6 +56,7 @@ struct FwdParams {
   uint32_t drop_threshold;  // floor(p * 2^32)
   float drop_rescale;       // 1 / (1 - p)
   PhiloxKey pk;
+  PhiloxRoundKeys rk;       // round keys of pk.k0, pk.k1 (used when rng_dev is null)
   const uint64_t* rng_dev;  // device {seed, offset} overriding pk, or null
   int b0, h0, H_total;      // counter position of this launch in the whole problem
   AttnBias bias;

@@ -50,6 +50,45 @@ __device__ __forceinline__ uint4 philox_group(uint64_t g, const PhiloxKey& pk) {
                        pk.off_hi, pk.k0, pk.k1);
 }
 
+// The ten round keys of a key (seed): words 2r and 2r+1 are the key of round r.
+struct PhiloxRoundKeys {
+  uint32_t w[20];
+};
+
+__host__ __device__ inline PhiloxRoundKeys philox_round_keys(const PhiloxKey& pk) {
+  PhiloxRoundKeys rk;
+  uint32_t k0 = pk.k0, k1 = pk.k1;
+  for (int r = 0; r < 10; ++r) {
+    rk.w[2 * r] = k0;
+    rk.w[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return rk;
+}
+
+// Group g drawn with round keys that the host formed and passed in the
+// kernel parameters: each round reads its key as a constant operand, so the
+// key schedule costs no registers and no additions (the same draws as
+// philox_group with the key the round keys came from).
+__device__ __forceinline__ uint4 philox_group_rk(uint64_t g, uint32_t off_lo, uint32_t off_hi,
+                                                 const PhiloxRoundKeys& rk) {
+  uint32_t c0 = static_cast<uint32_t>(g), c1 = static_cast<uint32_t>(g >> 32);
+  uint32_t c2 = off_lo, c3 = off_hi;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ c1 ^ rk.w[2 * r];
+    const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ c3 ^ rk.w[2 * r + 1];
+    c0 = n0;
+    c1 = static_cast<uint32_t>(pb);
+    c2 = n2;
+    c3 = static_cast<uint32_t>(pa);
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
 // Keep bits of the 32*W consecutive absolute indices n0 .. n0+32W-1:
 // bit e of bits[e/32] is 1 iff element n0+e is kept.
 template <int W>

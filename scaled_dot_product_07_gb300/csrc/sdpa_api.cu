@@ -348,6 +348,7 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
   p.drop_threshold = drop_threshold(dropout_p);
   p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
   p.pk = philox_key(seed, offset);
+  p.rk = philox_round_keys(p.pk);
   p.rng_dev = opt.rng;
   p.b0 = opt.b0;
   p.h0 = opt.h0;

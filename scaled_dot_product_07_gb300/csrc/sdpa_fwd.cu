@@ -144,7 +144,8 @@ __host__ __device__ constexpr bool fwd_two_items() {
 template <int D, bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+               const __grid_constant__ CUtensorMap tm_v,
+               const __grid_constant__ FwdParams p) {
   using L = FwdLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(320, 1)
           // 1/(1-p) is applied to O in the epilogue. The row sum takes P.
           float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
           uint32_t pk2[32];
-          // mode 0: no dropout; 1: the half row starts on a group boundary
+          // mode 0: no dropout; 1, 3: the half row starts on a group boundary
           // (Sk a multiple of 4), so group g_row + t holds keys 4t .. 4t+3 and
           // is drawn where those keys are exponentiated; 2: keep bits first
           auto exp_pack = [&](auto mode_c, uint64_t g_row, const uint32_t(&keep)[2]) {
@@ -489,8 +490,12 @@ __global__ void __launch_bounds__(320, 1)
   #pragma unroll
               for (int w = 0; w < 4; ++w) e[w] = ex2_approx(fmaf(x[c + w], sl2, neg));
               rs[(c >> 2) & 7] += (e[0] + e[1]) + (e[2] + e[3]);
-              if constexpr (kMode == 1) {
-                const uint4 u = philox_group(g_row + (c >> 2), pk);
+              if constexpr (kMode == 1 || kMode == 3) {
+                // 1: round keys from the kernel parameters; 3: from the key
+                // read out of device memory
+                const uint4 u = kMode == 1
+                                    ? philox_group_rk(g_row + (c >> 2), p.pk.off_lo, p.pk.off_hi, p.rk)
+                                    : philox_group(g_row + (c >> 2), pk);
                 const uint32_t thr = p.drop_threshold;
                 e[0] = u.x >= thr ? e[0] : 0.f;
                 e[1] = u.y >= thr ? e[1] : 0.f;
@@ -513,7 +518,10 @@ __global__ void __launch_bounds__(320, 1)
                                     static_cast<uint64_t>(p.Sk_ctr) +
                                 k0;
             if ((p.Sk_ctr & 3) == 0) {
-              exp_pack(std::integral_constant<int, 1>{}, n0 >> 2, no_bits);
+              if (p.rng_dev == nullptr)
+                exp_pack(std::integral_constant<int, 1>{}, n0 >> 2, no_bits);
+              else
+                exp_pack(std::integral_constant<int, 3>{}, n0 >> 2, no_bits);
             } else {
               uint32_t keep[2];
               keep_bits<2>(n0, p.drop_threshold, pk, keep);
