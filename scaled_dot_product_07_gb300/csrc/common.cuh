@@ -55,6 +55,7 @@ struct FwdParams {
   float scale_log2;       // softmax scale * log2(e)
   uint32_t drop_threshold;  // floor(p * 2^32)
   float drop_rescale;       // 1 / (1 - p)
+  int two_items;            // CTAs run items c and total-1-c (else one item each)
   PhiloxKey pk;
   PhiloxRoundKeys rk;       // round keys of pk.k0, pk.k1 (used when rng_dev is null)
   const uint64_t* rng_dev;  // device {seed, offset} overriding pk, or null
@@ -154,6 +155,22 @@ cudaError_t ensure_smem_attr(int bytes) {
   e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
   return e;
+}
+
+// SMs of the current device, queried once per device (0 on error).
+inline int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cached) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // Launchers (defined in the .cu files). Each returns the launch's CUDA error.

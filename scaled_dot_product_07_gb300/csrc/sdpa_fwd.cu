@@ -133,9 +133,10 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
   return it;
 }
 
-// Whether a variant runs two items per CTA (else one). With a bias the
+// Whether a variant can run two items per CTA (else one). With a bias the
 // second item's state and the prefetched bias words spill registers, and one
-// item per CTA is faster (1.29 against 1.34 ms at B8 H16 S4096 causal).
+// item per CTA is faster (1.29 against 1.34 ms at B8 H16 S4096 causal). The
+// launcher also keeps one item per CTA for grids of at most two items per SM.
 template <bool DROPOUT, bool BIAS, bool VARLEN>
 __host__ __device__ constexpr bool fwd_two_items() {
   return !BIAS;
@@ -173,11 +174,11 @@ __global__ void __launch_bounds__(320, 1)
   // long causal tile pairs of one window are matched with the short ones of
   // the other, so every CTA gets about the same work, and the second item's
   // Q and first K/V tiles load while the first item finishes.
-  constexpr bool kTwo = fwd_two_items<DROPOUT, BIAS, VARLEN>();
+  const bool two = fwd_two_items<DROPOUT, BIAS, VARLEN>() && p.two_items != 0;
   const int total = p.n_q_tiles * p.B * p.H;
   const int first_item = blockIdx.x;
-  const int second_item = kTwo ? total - 1 - static_cast<int>(blockIdx.x) : 0;
-  const int n_items = (kTwo && second_item > first_item) ? 2 : 1;
+  const int second_item = two ? total - 1 - static_cast<int>(blockIdx.x) : 0;
+  const int n_items = (two && second_item > first_item) ? 2 : 1;
   auto item_id = [&](int k) { return k == 0 ? first_item : second_item; };
 
   if (threadIdx.x == 0) {
@@ -596,8 +597,11 @@ cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream
   if (e != cudaSuccess) return e;
   // one or two items (query-tile pairs) per CTA
   const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
-  const unsigned grid = fwd_two_items<DR, BI, VL>() ? (items + 1) / 2 : items;
-  kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], p);
+  FwdParams pl = p;
+  pl.two_items = fwd_two_items<DR, BI, VL>() &&
+                 items > 2u * static_cast<unsigned>(device_sm_count());
+  const unsigned grid = pl.two_items ? (items + 1) / 2 : items;
+  kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], pl);
   return cudaGetLastError();
 }
 
