@@ -124,8 +124,8 @@ struct WaitCtl {
   uint64_t limit_ns;
 };
 
-static __device__ __noinline__ void mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
-                                            uint32_t site) {
+__device__ __forceinline__ void mbar_wait_poll(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
+                                               uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return;
@@ -138,10 +138,30 @@ static __device__ __noinline__ void mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
 }
 
+
+static __device__ __noinline__ void mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
+                                            uint32_t site) {
+  mbar_wait_poll(bar, parity, wc, site);
+}
+
+// The polling loop sits out of line (a call) in mbar_wait, which keeps the
+// code of kernels with many waits small, and inline in mbar_wait_t<true>: a
+// call makes the caller spill the registers it keeps live across it, which
+// costs the kernels whose loops are short of registers.
 __device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return;
   mbar_wait_slow(bar, parity, wc, site);
+}
+
+template <bool kInline>
+__device__ __forceinline__ void mbar_wait_t(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
+                                            uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return;
+  if constexpr (kInline)
+    mbar_wait_poll(bar, parity, wc, site);
+  else
+    mbar_wait_slow(bar, parity, wc, site);
 }
 
 // A wait used only while shutting down: bounded, and it ignores the abort flag.

@@ -93,6 +93,10 @@ __global__ void __launch_bounds__(448, 1)
                          const __grid_constant__ CUtensorMap tm_dbias, const BwdParams p) {
   using L = B128<BIAS>;
   constexpr int NS = L::kStages;
+  // waits poll inline in the variants whose compute loops are short of
+  // registers (dropout, bias, packed batches: spills around the call of an
+  // out-of-line poll); the plain variants keep the smaller out-of-line form
+  constexpr bool kInlineWaits = DROPOUT || BIAS || VARLEN;
   constexpr int MQ = L::kMq;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -187,10 +191,10 @@ __global__ void __launch_bounds__(448, 1)
       for (int t = 0; t < n_steps; ++t) {
         const int st = t % NS;
         const int i0 = (qt_first + t) * MQ;
-        if (t >= NS) mbar_wait(&q_empty[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
+        if (t >= NS) mbar_wait_t<kInlineWaits>(&q_empty[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
         // the bias stage also held step t-NS's dbias tile until its store read it
         if (BIAS && p.dbias.data != nullptr && t >= NS)
-          mbar_wait(&dbias_read[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
+          mbar_wait_t<kInlineWaits>(&dbias_read[st], ((t / NS) - 1) & 1, wc, kSiteBwdQEmpty);
         mbar_arrive_expect_tx(&q_full[st],
                               2 * L::kQBytes + 2 * MQ * 4 + (BIAS ? L::kBiasBytes : 0));
 #pragma unroll
@@ -234,14 +238,14 @@ __global__ void __launch_bounds__(448, 1)
         const uint64_t d_omn = sdesc_sw128(sb + L::kDO + st * L::kQBytes, L::kQSlab, 1024);
         const uint64_t d_ds = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, 16, 1024);
         const uint64_t d_dsmn = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, L::kDsBytes, 1024);
-        mbar_wait(&p_full[x], (u >> 1) & 1, wc, kSiteBwdPFull);
+        mbar_wait_t<kInlineWaits>(&p_full[x], (u >> 1) & 1, wc, kSiteBwdPFull);
         tc_fence_after();
         // dV += P~^T dO: A = P~^T bf16 in TMEM (32 columns), B = dO MN-major
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk)
           mma_bf16_ts_if(leader, tmem + L::kTmemDV, tmem + L::tmem_s(x) + kk * 8,
                          sdesc_add(d_omn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
-        mbar_wait(&ds_full[x], (u >> 1) & 1, wc, kSiteBwdDsFull);
+        mbar_wait_t<kInlineWaits>(&ds_full[x], (u >> 1) & 1, wc, kSiteBwdDsFull);
         tc_fence_after();
         // dK += dS^T Q: A = dS^T smem K-major, B = Q MN-major
 #pragma unroll
@@ -260,15 +264,15 @@ __global__ void __launch_bounds__(448, 1)
         mma_commit_if(leader, &q_empty[st]);
         mma_commit_if(leader, &ds_empty[x]);
       };
-      mbar_wait(kv_full, 0, wc, kSiteBwdKvFull);
+      mbar_wait_t<kInlineWaits>(kv_full, 0, wc, kSiteBwdKvFull);
       for (int t = 0; t < n_steps; ++t) {
         const int x = t & 1;
         const int st = t % NS;
         const uint64_t d_q = sdesc_sw128(sb + L::kQ + st * L::kQBytes, 16, 1024);
         const uint64_t d_o = sdesc_sw128(sb + L::kDO + st * L::kQBytes, 16, 1024);
-        mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
+        mbar_wait_t<kInlineWaits>(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
         // step buffer x: S^T(t-2) and dP^T(t-2) read by the compute warpgroup
-        if (t >= 2) mbar_wait(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
+        if (t >= 2) mbar_wait_t<kInlineWaits>(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
         tc_fence_after();
         // S^T = K Q^T and dP~^T = V dO^T  (M = 128 keys, N = MQ, K = D)
 #pragma unroll
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(448, 1)
         mma_commit_if(leader, &s_full[x]);
         // the dP^T columns held dQ^T(t-2) until the dQ warpgroup read it out
         if (t >= 2) {
-          mbar_wait(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
+          mbar_wait_t<kInlineWaits>(&dq_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdDqEmpty);
           tc_fence_after();
         }
 #pragma unroll
@@ -335,8 +339,8 @@ __global__ void __launch_bounds__(448, 1)
           }
         }
       }
-      mbar_wait(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
-      mbar_wait(&s_full[x], k & 1, wc, kSiteBwdSFull);
+      mbar_wait_t<kInlineWaits>(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
+      mbar_wait_t<kInlineWaits>(&s_full[x], k & 1, wc, kSiteBwdSFull);
       tc_fence_after();
       float pv[MQ];
       {
@@ -380,9 +384,9 @@ __global__ void __launch_bounds__(448, 1)
       tc_fence_before();
       mbar_arrive(&p_full[x]);
 
-      mbar_wait(&dp_full[x], k & 1, wc, kSiteBwdDpFull);
+      mbar_wait_t<kInlineWaits>(&dp_full[x], k & 1, wc, kSiteBwdDpFull);
       tc_fence_after();
-      if (k >= 1) mbar_wait(&ds_empty[x], (k - 1) & 1, wc, kSiteBwdPdsEmpty);
+      if (k >= 1) mbar_wait_t<kInlineWaits>(&ds_empty[x], (k - 1) & 1, wc, kSiteBwdPdsEmpty);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t d[32];
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(448, 1)
     for (int t = 0; t < n_steps; ++t) {
       const int x = t & 1;
       const int i0 = (qt_first + t) * MQ;
-      mbar_wait(&dq_full[x], (t >> 1) & 1, wc, kSiteBwdDqFull);
+      mbar_wait_t<kInlineWaits>(&dq_full[x], (t >> 1) & 1, wc, kSiteBwdDqFull);
       tc_fence_after();
       uint32_t r0[32], r1[32];
       tmem_ld32(tmem + L::tmem_dp(x) + lane_base, r0);
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(448, 1)
     // of the next sequence are never written (uniform over the CTA)
     const bool direct = VARLEN && (k0 + 128 > Sk);
     if (n_steps > 0) {
-      mbar_wait(done, 0, wc, kSiteBwdDone);
+      mbar_wait_t<kInlineWaits>(done, 0, wc, kSiteBwdDone);
       tc_fence_after();
     }
 #pragma unroll
