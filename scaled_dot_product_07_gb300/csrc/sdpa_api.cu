@@ -219,6 +219,11 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 // those of the unpadded problem.
 bool head_dim_supported(int64_t D) { return D >= 8 && D <= 128 && D % 8 == 0; }
 int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+// The backward runs every head dim on the 128-wide kernel: at D=64 it beat a
+// 64-wide kernel of 128-row query steps (B8 H16 S4096 causal: 1.31 against
+// 1.41 ms; with dropout 0.1: 2.05 against 4.53 ms). The fp32 dQ rows of the
+// workspace are therefore 128 wide for every D.
+constexpr int64_t kBwdHeadDim = 128;
 
 // Resolved sdpa_options.
 struct Opts {
@@ -382,7 +387,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
                        sdpa_tensor* dk, sdpa_tensor* dv, void* workspace, size_t workspace_bytes,
                        const sdpa_options* options, const Opts& opt, const int32_t* cu_q,
                        const int32_t* cu_k, int64_t total_q, cudaStream_t stream) {
-  const int64_t Dk = kernel_head_dim(D);
+  const int64_t Dk = kBwdHeadDim;
   const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SDPA_ERR_WORKSPACE;
@@ -572,7 +577,7 @@ size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
   const int64_t Sq_pad = round_up(Sq, 128);
-  return static_cast<size_t>(B * H * Sq_pad * (kernel_head_dim(D) + 2) * 4);
+  return static_cast<size_t>(B * H * Sq_pad * (kBwdHeadDim + 2) * 4);
 }
 
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
@@ -581,7 +586,7 @@ size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
   const int64_t Sq_pad = round_up(Sq, 128);
   const int64_t n_kv = (Sk + 127) / 128;
-  return static_cast<size_t>(B * H * Sq_pad * (kernel_head_dim(D) * n_kv + 2) * 4);
+  return static_cast<size_t>(B * H * Sq_pad * (kBwdHeadDim * n_kv + 2) * 4);
 }
 
 sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
@@ -596,7 +601,6 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
   if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
-  const int64_t Dk = kernel_head_dim(D);
   if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;

@@ -522,9 +522,10 @@ __global__ void __launch_bounds__(448, 1)
       named_barrier_sync(is_dv ? 3 : 4, 128);
       if (r == 0) {
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
-          tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
-                       s * 64, ks + k0, h, tb);
+        for (int s = 0; s < 2; ++s)  // column slabs the caller's head dim reaches
+          if (s * 64 < p.D_io)
+            tma_store_4d(is_dv ? &tm_dv : &tm_dk, smem + (is_dv ? L::kK : L::kV) + s * L::kKvSlab,
+                         s * 64, ks + k0, h, tb);
         bulk_commit();
         bulk_wait_all();
       }

@@ -55,11 +55,11 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     import scaled_dot_product_07_gb300 as sdpa
     # fp32 dQ accumulator + two fp32 row vectors, Sq rounded up to 128
-    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (64 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(8, 16, 4096, 4096, 128) == 8 * 16 * 4096 * 130 * 4
     assert sdpa.sdpa_bwd_workspace_size(0, 3, 200, 77, 64) == 0
-    # a head dim below 64 (128) uses the 64-wide (128-wide) accumulator rows
-    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (64 + 2) * 4
+    # the backward runs every head dim on 128-wide tiles: 128-wide accumulator rows
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 96) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(1, 1, 0, 77, 64) == 0
 
@@ -182,7 +182,7 @@ def options(**kw):
 def test_deterministic_workspace_holds_one_dq_slice_per_key_tile(lib):
     import scaled_dot_product_07_gb300 as sdpa
     # one fp32 [B*H, ceil128(Sq), D] slice per 128-key tile, plus lse2 and delta
-    assert sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, True) == 2 * 3 * 256 * (64 * 3 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, True) == 2 * 3 * 256 * (128 * 3 + 2) * 4
     assert (sdpa.sdpa_bwd_workspace_size_ex(8, 16, 4096, 4096, 128, True)
             == 8 * 16 * 4096 * (128 * 32 + 2) * 4)
     # without the flag (or with no options at all) it is the plain workspace
