@@ -105,7 +105,7 @@ struct BwdParams {
 };
 
 
-// D is the kernels' head dim (64 or 128: the width of the fp32 dQ rows);
+// D is the backward kernel's head dim (128: the width of the fp32 dQ rows);
 // D_io the caller's head dim (a multiple of 8, at most D), the width of the
 // rows read from out / dout and written to dq.
 struct PreParams {

@@ -733,7 +733,7 @@ const char* sdpa_status_string(sdpa_status status) {
   switch (status) {
     case SDPA_OK: return "SDPA_OK";
     case SDPA_ERR_INVALID_ARG: return "SDPA_ERR_INVALID_ARG: invalid argument";
-    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported shape or layout (D must be 64 or 128, innermost)";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported shape or layout (D a multiple of 8 in [8, 128], innermost)";
     case SDPA_ERR_ALIGNMENT: return "SDPA_ERR_ALIGNMENT: base pointers and strides must be 16-byte aligned";
     case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA: CUDA launch or driver call failed";
     case SDPA_ERR_DEVICE_TIMEOUT: return "SDPA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
