@@ -16,7 +16,7 @@
 //               stored as bf16 into shared memory (operand of dK and dQ).
 //   warps 8-11  dQ warpgroup: reads the dQ^T partial of a step from TMEM,
 //               stages it fp32 [64 x 128] and reduces it into the global fp32
-//               accumulator with one bulk reduce-add.
+//               accumulator with four bulk reduce-adds (one per warp).
 // TMEM (512 columns): dV [0,128), dK [128,256), and two step buffers
 // {S^T, dP^T} at [256,384) and [384,512). A step's dQ^T partial (M = D =
 // 128 lanes, 64 columns) overwrites its own dP^T columns, which the compute
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(448, 1)
       touch32(r1);
       tc_fence_before();
       mbar_arrive(&dq_empty[x]);
-      if (lt == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
+      if ((lt & 31) == 0) bulk_wait_read_all();  // the previous reduces have read the staging tile
       named_barrier_sync(2, 128);
       // lane = d, columns = query rows; the staging tile is row-major [MQ][D] fp32
 #pragma unroll
@@ -460,13 +460,16 @@ __global__ void __launch_bounds__(448, 1)
       }
       fence_async_smem();
       named_barrier_sync(2, 128);
-      if (lt == 0) {
-        dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0) * 128, smem + L::kDq,
-               L::kDqBytes);
+      if ((lt & 31) == 0) {
+        // each warp's first lane reduces a quarter of the tile (16 rows), so
+        // four bulk reduces are in flight at once
+        const int hh = lt >> 5;
+        dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0 + 16 * hh) * 128,
+               smem + L::kDq + hh * (L::kDqBytes / 4), L::kDqBytes / 4);
         bulk_commit();
       }
     }
-    if (lt == 0) bulk_wait_all();
+    if ((lt & 31) == 0) bulk_wait_all();
   }
 
   // ------------------------------------------------------------ epilogue: dV (A), dK (B)
