@@ -54,11 +54,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4f(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float a) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
@@ -275,28 +270,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T  (bf16 in, fp32 accumulate)
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Warp-converged issue: every lane of the MMA warp executes these with the
 // same (warp-uniform) operands, and only the lane whose `leader` is nonzero
 // issues. Keeping the warp converged lets descriptors live in uniform
@@ -311,6 +284,8 @@ __device__ __forceinline__ uint32_t elect_one() {
   return pred;
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T (bf16 in, fp32 accumulate; accumulate = 0
+// overwrites D)
 __device__ __forceinline__ void mma_bf16_ss_if(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
                                                uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -323,6 +298,7 @@ __device__ __forceinline__ void mma_bf16_ss_if(uint32_t leader, uint32_t d_tmem,
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T
 __device__ __forceinline__ void mma_bf16_ts_if(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
                                                uint64_t b_desc, uint32_t idesc,
                                                uint32_t accumulate) {
@@ -335,6 +311,7 @@ __device__ __forceinline__ void mma_bf16_ts_if(uint32_t leader, uint32_t d_tmem,
       : "memory");
 }
 
+// Arrive (once) on `bar` when every tcgen05 op the leader issued so far is done.
 __device__ __forceinline__ void mma_commit_if(uint32_t leader, uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred q;\n\t"
@@ -351,13 +328,6 @@ __device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
   return desc + (bytes >> 4);
 }
 
-// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 
 // 32 lanes x 32 consecutive 32-bit columns; thread t of the warp gets lane
 // (warp's lane quarter)+t. Results are valid only after tmem_ld_wait().
