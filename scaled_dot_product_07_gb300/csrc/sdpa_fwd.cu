@@ -40,6 +40,12 @@
 // (tcgen05 operations of one issuing thread complete in order), so the
 // softmax may touch O_i as soon as it sees its next scores.
 // Key tiles entirely above the causal diagonal are never loaded or computed.
+// Small grids (at most two items per SM) run one item per CTA.
+//
+// With an additive bias the forward is fwd_kernel_bias: the same roles and
+// products, one item per CTA, each softmax thread's 64 bias values fetched
+// with 16-byte loads before its scores are ready, out staged in the dead Q
+// tiles and stored by TMA.
 #include <type_traits>
 
 #include "common.cuh"
@@ -133,16 +139,7 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
   return it;
 }
 
-// Whether a variant can run two items per CTA (else one). With a bias the
-// second item's state and the prefetched bias words spill registers, and one
-// item per CTA is faster (1.29 against 1.34 ms at B8 H16 S4096 causal). The
-// launcher also keeps one item per CTA for grids of at most two items per SM.
-template <bool DROPOUT, bool BIAS, bool VARLEN>
-__host__ __device__ constexpr bool fwd_two_items() {
-  return !BIAS;
-}
-
-template <int D, bool CAUSAL, bool DROPOUT, bool BIAS, bool VARLEN>
+template <int D, bool CAUSAL, bool DROPOUT, bool VARLEN>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v,
@@ -174,7 +171,7 @@ __global__ void __launch_bounds__(320, 1)
   // long causal tile pairs of one window are matched with the short ones of
   // the other, so every CTA gets about the same work, and the second item's
   // Q and first K/V tiles load while the first item finishes.
-  const bool two = fwd_two_items<DROPOUT, BIAS, VARLEN>() && p.two_items != 0;
+  const bool two = p.two_items != 0;
   const int total = p.n_q_tiles * p.B * p.H;
   const int first_item = blockIdx.x;
   const int second_item = two ? total - 1 - static_cast<int>(blockIdx.x) : 0;
@@ -382,35 +379,6 @@ __global__ void __launch_bounds__(320, 1)
           const int qi = q0 + 128 * i + row;
           const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
           const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-          // the half row's 64 bias values, fetched before the scores are ready
-          uint4 bv[8];
-          if (BIAS) {
-            // start the next key tile's bias line towards L2
-            const int kn = (j + 1) * 128 + 64 * half;
-            if (j + 1 < n_t[i] && kn < Sk) {
-              const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                                   static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
-              prefetch_l2(np);
-              prefetch_l2(np + min(56, Sk - 1 - kn));
-            }
-            const int kb = j * 128 + 64 * half;
-            const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
-  #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              if (kb + 8 * c + 8 <= Sk) {
-                bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
-              } else {
-                // key tail: only the keys that exist are read
-                uint32_t w[4] = {0u, 0u, 0u, 0u};
-  #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  if (kb + 8 * c + e < Sk)
-                    w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
-                bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
-          }
           mbar_wait(&s_full[i], sc[i] & 1, wc, kSiteFwdSFull);
           ++sc[i];
           tc_fence_after();
@@ -424,19 +392,6 @@ __global__ void __launch_bounds__(320, 1)
           for (int c = 0; c < 32; ++c) {
             x[c] = __uint_as_float(r0[c]);
             x[32 + c] = __uint_as_float(r1[c]);
-          }
-          if (BIAS) {
-            // the bias in raw-score units (scores are scaled at the exponential)
-            const float inv = p.bias_to_raw;
-  #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t w[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
-  #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                x[8 * c + 2 * e] = fmaf(bf16_bits_to_float(w[e] & 0xffffu), inv, x[8 * c + 2 * e]);
-                x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
-              }
-            }
           }
           const int k0 = j * 128 + 64 * half;  // first key of this half
           if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
@@ -589,19 +544,428 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool C, bool DR, bool BI, bool VL>
+// The forward with an additive bias: one item (query-tile pair) per CTA, O
+// staged in the dead Q tiles and stored by TMA. The same algorithm as
+// fwd_kernel; kept as its own kernel because with a bias it runs 1.19 ms
+// against fwd_kernel's 1.38 (B8 H16 S4096 D128 causal, relative-position
+// bias [1,H,S,S]). Packed batches take no bias, so it has no packed form.
+template <int D, bool CAUSAL, bool DROPOUT>
+__global__ void __launch_bounds__(320, 1)
+    fwd_kernel_bias(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+  constexpr bool BIAS = true;
+  using L = FwdLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + S;
+  uint64_t* k_empty = v_full + S;
+  uint64_t* v_empty = k_empty + S;
+  uint64_t* s_full = v_empty + S;    // [2]
+  uint64_t* p_full = s_full + 2;     // [2]
+  uint64_t* o_full = p_full + 2;     // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // head-major order (a head's K/V stays in L2 while its tiles run);
+  // within a head the longest causal tiles go first
+  const int n_pairs = p.n_q_tiles;  // tile pairs per head
+  const int slot = blockIdx.x / n_pairs;
+  int pair = blockIdx.x - slot * n_pairs;
+  if (CAUSAL) pair = n_pairs - 1 - pair;
+  // (b, h) of this CTA: batch-major, or head-major when a bias shared by the
+  // batch makes the batches of one head read the same bias tiles
+  const int b = p.h_major ? slot % p.B : slot / p.H;
+  const int h = p.h_major ? slot / p.B : slot - b * p.H;
+  const int bh = b * p.H + h;
+  const int q0 = pair * 256;
+  const int Sq = p.Sq, Sk = p.Sk, qs = 0, ks = 0;
+  const int tb = b;  // batch coordinate in the tensor maps
+  const int n_t[2] = {kv_tiles_for(q0, Sq, Sk, CAUSAL), kv_tiles_for(q0 + 128, Sq, Sk, CAUSAL)};
+  const int n_kv = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 256);
+      mbar_init(&o_full[i], 1);
+    }
+    *abort_word = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(tmem_holder, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const WaitCtl wc{abort_word, p.err, p.wait_limit_ns};
+
+  if (warp == 9) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const int nq = n_t[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq * L::kTileBytes);
+      for (int i = 0; i < nq; ++i) {
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, &tm_q, q_full, s * 64,
+                      qs + q0 + 128 * i, h, tb);
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % S;
+        // a K stage is free once the last S MMA reading it is done, a V stage
+        // once the last P V MMA reading it is done
+        if (j >= S) mbar_wait(&k_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
+        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kK + st * L::kTileBytes + s * L::kSlabBytes, &tm_k, &k_full[st],
+                      s * 64, ks + j * 128, h, tb);
+        if (j >= S) mbar_wait(&v_empty[st], ((j / S) - 1) & 1, wc, kSiteFwdKvEmpty);
+        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem + L::kV + st * L::kTileBytes + s * L::kSlabBytes, &tm_v, &v_full[st],
+                      s * 64, ks + j * 128, h, tb);
+      }
+      if (*abort_word) {
+        // give the loads still in flight time to land before the CTA exits
+        for (int j = max(0, n_kv - S); j < n_kv; ++j) {
+          mbar_wait_drain(&k_full[j % S], (j / S) & 1, 2000000ull);
+          mbar_wait_drain(&v_full[j % S], (j / S) & 1, 2000000ull);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 8) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp runs this loop (waits and descriptor arithmetic are
+    // warp-uniform); one elected lane issues the tcgen05 instructions.
+    const uint32_t leader = elect_one();
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+    auto issue_s = [&](int i, int j) {
+      const int st = j % S;
+      const uint64_t qd = sdesc_sw128(sb + L::kQ + i * L::kTileBytes, 16, 1024);
+      const uint64_t kd = sdesc_sw128(sb + L::kK + st * L::kTileBytes, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * L::kSlabBytes + (kk & 3) * 32;
+        mma_bf16_ss_if(leader, tmem + L::tmem_s(i), sdesc_add(qd, koff), sdesc_add(kd, koff), kIdS,
+                       kk > 0 ? 1u : 0u);
+      }
+      mma_commit_if(leader, &s_full[i]);
+    };
+    auto issue_pv = [&](int i, int j) {
+      const int st = j % S;
+      const uint64_t vd = sdesc_sw128(sb + L::kV + st * L::kTileBytes, L::kSlabBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_bf16_ts_if(leader, tmem + L::tmem_o(i), tmem + L::tmem_s(i) + kk * 8,
+                       sdesc_add(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    mbar_wait(q_full, 0, wc, kSiteFwdQFull);
+    if (n_kv > 0) {
+      mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+      tc_fence_after();
+      for (int i = 0; i < 2; ++i)
+        if (n_t[i] > 0) issue_s(i, 0);
+      mma_commit_if(leader, &k_empty[0]);  // K_0 has no other reader
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      const int st = j % S;
+      mbar_wait(&v_full[st], (j / S) & 1, wc, kSiteFwdKvFull);
+      for (int i = 0; i < 2; ++i) {
+        if (j >= n_t[i]) continue;
+        mbar_wait(&p_full[i], j & 1, wc, kSiteFwdPFull);
+        tc_fence_after();
+        issue_pv(i, j);
+        if (j + 1 < n_t[i]) {
+          const int st1 = (j + 1) % S;
+          mbar_wait(&k_full[st1], ((j + 1) / S) & 1, wc, kSiteFwdKvFull);
+          tc_fence_after();
+          issue_s(i, j + 1);
+        } else {
+          mma_commit_if(leader, &o_full[i]);
+        }
+      }
+      mma_commit_if(leader, &v_empty[st]);                             // V_j read by both P V
+      if (j + 1 < n_kv) mma_commit_if(leader, &k_empty[(j + 1) % S]);  // K_{j+1} by both S
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    // Both warpgroups work on the same tile: warp w and warp w+4 share TMEM
+    // lanes, so thread (half, r) handles key columns [64h, 64h+64) of query row
+    // r. The two halves of a row agree on its max through shared memory and
+    // a 64-thread named barrier per warp pair; their partial row sums are
+    // combined only at the end.
+    const int half = warp >> 2;         // half of the key columns
+    const int row = threadIdx.x & 127;  // row in the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t pair_bar = 1 + (warp & 3);  // + 4 * tile
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
+    const float sl2 = p.scale_log2;
+    const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
+    float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
+    float l[2] = {0.f, 0.f};              // this half's running sum, per tile
+    // the half's tile max, shared with the partner half; returns the row's tile max
+    auto exchange_max = [&](int i, int j, float mh) {
+      float* slot = red + ((i * 2 + (j & 1)) * 2) * 128;
+      slot[half * 128 + row] = mh;
+      // also orders the partner's TMEM score reads before this warp's P
+      // stores into the same columns
+      tc_fence_before();
+      named_barrier_sync(pair_bar + 4 * i, 64);
+      tc_fence_after();
+      return fmaxf(mh, slot[(1 - half) * 128 + row]);
+    };
+
+    for (int j = 0; j < n_kv; ++j) {
+      for (int i = 0; i < 2; ++i) {
+        if (j >= n_t[i]) continue;
+        const int qi = q0 + 128 * i + row;
+        const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
+        const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+        // the half row's 64 bias values, fetched before the scores are ready
+        uint4 bv[8];
+        if (BIAS) {
+          // start the next key tile's bias line towards L2
+          const int kn = (j + 1) * 128 + 64 * half;
+          if (j + 1 < n_t[i] && kn < Sk) {
+            const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
+            prefetch_l2(np);
+            prefetch_l2(np + min(56, Sk - 1 - kn));
+          }
+          const int kb = j * 128 + 64 * half;
+          const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                               static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (kb + 8 * c + 8 <= Sk) {
+              bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
+            } else {
+              // key tail: only the keys that exist are read
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (kb + 8 * c + e < Sk)
+                  w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
+              bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+        mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tS + 64 * half, r0);
+        tmem_ld32(tS + 64 * half + 32, r1);
+        tmem_ld_wait(r0);
+        reg_touch(r1);
+        float x[64];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0[c]);
+          x[32 + c] = __uint_as_float(r1[c]);
+        }
+        if (BIAS) {
+          // the bias in raw-score units (scores are scaled at the exponential)
+          const float inv = p.bias_to_raw;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t w[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              x[8 * c + 2 * e] = fmaf(bf16_bits_to_float(w[e] & 0xffffu), inv, x[8 * c + 2 * e]);
+              x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
+            }
+          }
+        }
+        const int k0 = j * 128 + 64 * half;  // first key of this half
+        if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
+          const int lim = CAUSAL ? min(Sk - k0, qi - k0 + 1) : (Sk - k0);
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c >= lim) x[c] = -INFINITY;
+        }
+        // half-row max as 8 independent chains, then combined
+        float mp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(x[2 * u], x[2 * u + 1]);
+#pragma unroll
+        for (int c = 16; c < 64; c += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[c + 2 * u], x[c + 2 * u + 1]);
+        const float mh =
+            fmaxf(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], fmax3(mp[5], mp[6], mp[7])));
+        const float m_new = fmaxf(m[i], exchange_max(i, j, mh));
+        if (j == 0) {
+          m[i] = m_new;
+        } else if (__any_sync(0xffffffffu, (m_new - m[i]) * sl2 > 8.0f)) {
+          // both halves of these rows take this branch (same rows, same maxima);
+          // O_i += P_i(j-1) V has completed (S_i(j) completed after it)
+          const float alpha = ex2_approx((m[i] - m_new) * sl2);
+          l[i] *= alpha;
+          m[i] = m_new;
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
+            uint32_t o[32];
+            tmem_ld32(tO + (D / 2) * half + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + (D / 2) * half + c * 32, o);
+          }
+        }
+        const float neg = -m[i] * sl2;
+
+        uint32_t keep[2] = {0xffffffffu, 0xffffffffu};
+        if (DROPOUT) {
+          const uint64_t n_row = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + qi) *
+                                 static_cast<uint64_t>(p.Sk_ctr);
+          keep_bits<2>(n_row + k0, p.drop_threshold, pk, keep);
+        }
+        // the same arithmetic as fwd_kernel: partial sums four keys at a time,
+        // P~ = keep ? P : 0, and 1/(1-p) applied with 1/l in the epilogue
+        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
+        uint32_t pk2[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          float e[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) e[w] = ex2_approx(fmaf(x[c + w], sl2, neg));
+          rs[(c >> 2) & 7] += (e[0] + e[1]) + (e[2] + e[3]);
+          if (DROPOUT) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+              e[w] = ((keep[(c + w) >> 5] >> ((c + w) & 31)) & 1u) ? e[w] : 0.f;
+          }
+          pk2[c >> 1] = pack_bf16x2(e[0], e[1]);
+          pk2[(c >> 1) + 1] = pack_bf16x2(e[2], e[3]);
+        }
+        // P (bf16 pairs) of keys [64h, 64h+64) -> S columns [32h, 32h+32); they
+        // overwrite scores this warp pair has already read
+        tmem_st32(tS + 32 * half, pk2);
+        l[i] += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[i]);
+      }
+    }
+
+    // ------------------------------------------------------------ epilogue
+    for (int i = 0; i < 2; ++i) {
+      if (n_t[i] == 0) continue;
+      const int qi = q0 + 128 * i + row;
+      const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
+      // the row sum is the sum of both halves (slot parity n_t[i] is unused by
+      // the last tile's max exchange)
+      const float l_row = [&] {
+        float* slot = red + ((i * 2 + (n_t[i] & 1)) * 2) * 128;
+        slot[half * 128 + row] = l[i];
+        named_barrier_sync(pair_bar + 4 * i, 64);
+        return l[i] + slot[(1 - half) * 128 + row];
+      }();
+      mbar_wait(&o_full[i], 0, wc, kSiteFwdODone);
+      tc_fence_after();
+      // 1/l, and the dropout rescale 1/(1-p) of the kept weights
+      const float inv_l = (DROPOUT ? p.drop_rescale : 1.f) / l_row;
+      const uint32_t oa = sb + L::kQ + i * L::kTileBytes;  // Q_i is dead after o_full[i]
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns
+        uint32_t o[32];
+        tmem_ld32(tO + (D / 2) * half + c * 32, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int col0 = (D / 2) * half + c * 32 + q4 * 8;
+          const uint32_t w0 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+          const uint32_t w1 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+          const uint32_t w2 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+          const uint32_t w3 = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l,
+                                          __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+          st_shared_v4(oa + (col0 >> 6) * L::kSlabBytes + sw128_offset(row, (col0 & 63) >> 3),
+                       w0, w1, w2, w3);
+        }
+      }
+      if (half == 0 && qi < Sq)
+        p.lse[static_cast<size_t>(bh) * Sq + qi] = m[i] * (sl2 * kLn2) + __logf(l_row);
+      // rows past Sq and columns past D_io are clipped by the store
+      fence_async_smem();
+      named_barrier_sync(9 + i, 256);
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_store_4d(&tm_o, smem + L::kQ + i * L::kTileBytes + s * L::kSlabBytes, s * 64,
+                       qs + q0 + 128 * i, h, tb);
+        bulk_commit();
+        bulk_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+
+
+// Two items per CTA once there are more than two items per SM, else one.
+template <int D, bool C, bool DR, bool VL>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<D, C, DR, BI, VL>;
+  auto kern = fwd_kernel<D, C, DR, VL>;
   const int smem = FwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, BI, VL>>(smem);
+  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, VL>>(smem);
   if (e != cudaSuccess) return e;
-  // one or two items (query-tile pairs) per CTA
   const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
   FwdParams pl = p;
-  pl.two_items = fwd_two_items<DR, BI, VL>() &&
-                 items > 2u * static_cast<unsigned>(device_sm_count());
+  pl.two_items = items > 2u * static_cast<unsigned>(device_sm_count());
   const unsigned grid = pl.two_items ? (items + 1) / 2 : items;
   kern<<<grid, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], pl);
+  return cudaGetLastError();
+}
+
+// One item per CTA.
+template <int D, bool C, bool DR>
+cudaError_t launch_fwd_bias_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
+  auto kern = fwd_kernel_bias<D, C, DR>;
+  const int smem = FwdLayout<D>::kAlloc;
+  cudaError_t e = ensure_smem_attr<fwd_kernel_bias<D, C, DR>>(smem);
+  if (e != cudaSuccess) return e;
+  const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
+  kern<<<items, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaGetLastError();
 }
 
@@ -617,9 +981,9 @@ cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps
   const bool varlen = p.cu_q != nullptr;  // packed batches take no bias
 #define SDPA_FWD_CASE(DD, CC, RR)                                                    \
   if (D == DD && causal == CC && dropout == RR)                                      \
-    return varlen ? launch_fwd_t<DD, CC, RR, false, true>(maps, p, stream)           \
-                  : (bias ? launch_fwd_t<DD, CC, RR, true, false>(maps, p, stream)   \
-                          : launch_fwd_t<DD, CC, RR, false, false>(maps, p, stream));
+    return varlen ? launch_fwd_t<DD, CC, RR, true>(maps, p, stream)                  \
+                  : (bias ? launch_fwd_bias_t<DD, CC, RR>(maps, p, stream)           \
+                          : launch_fwd_t<DD, CC, RR, false>(maps, p, stream));
   SDPA_FWD_CASE(64, false, false)
   SDPA_FWD_CASE(64, false, true)
   SDPA_FWD_CASE(64, true, false)
