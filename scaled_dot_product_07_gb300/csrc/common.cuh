@@ -179,10 +179,10 @@ cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps
 cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout,
-                            const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
+                            const CUtensorMap* maps /*q,k,v,do,dk,dv,bias,dbias,dq*/, const BwdParams& p,
                             cudaStream_t stream);
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout,
-                                 const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
+                                 const CUtensorMap* maps /*q,k,v,do,dk,dv,bias,dbias,dq*/, const BwdParams& p,
                                  cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStream_t stream);

@@ -168,6 +168,22 @@ bool make_map(CUtensorMap* m, const sdpa_tensor* t, uint32_t box_rows) {
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map of the fp32 dQ accumulator as a [rows, 128] matrix (rows =
+// B*H*Sq_pad): box [64 rows x 32 columns], the columns one dQ warp of the
+// backward holds for a 64-row query step; no swizzle.
+bool make_dq_map(CUtensorMap* m, float* acc, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128 * 4};
+  cuuint32_t box[2] = {32, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tensor map of an attention bias [Bb, Hb, Sq, Sk] (keys contiguous) for the
 // backward's bias tiles: box [64 query rows x 128 keys], no swizzle, zeros
 // past the edges. A shared (size-1) dim is always read at coordinate 0, so
@@ -402,12 +418,15 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   float* dq_acc = opt.det ? nullptr : dq_region;
 
   const uint32_t mq = static_cast<uint32_t>(8192 / Dk);
-  CUtensorMap maps[8];  // q, k, v, dout, dk, dv, bias, dbias (copies of q's when absent)
+  // q, k, v, dout, dk, dv, bias, dbias, dq accumulator (copies of q's when absent)
+  CUtensorMap maps[9];
   if (!make_map(&maps[0], q, mq) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
       !make_map(&maps[3], dout, mq) || !make_map(&maps[4], dk, 128) || !make_map(&maps[5], dv, 128))
     return SDPA_ERR_CUDA;
   maps[6] = maps[0];
   maps[7] = maps[0];
+  maps[8] = maps[0];
+  if (dq_acc != nullptr && !make_dq_map(&maps[8], dq_acc, B * H * Sq_pad)) return SDPA_ERR_CUDA;
   if (opt.bias.data != nullptr &&
       !make_bias_map(&maps[6], opt.bias, opt.bias_B, opt.bias_H, Sq, Sk))
     return SDPA_ERR_CUDA;

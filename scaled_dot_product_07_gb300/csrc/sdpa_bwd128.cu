@@ -90,7 +90,8 @@ __global__ void __launch_bounds__(448, 1)
                          const __grid_constant__ CUtensorMap tm_dk,
                          const __grid_constant__ CUtensorMap tm_dv,
                          const __grid_constant__ CUtensorMap tm_bias,
-                         const __grid_constant__ CUtensorMap tm_dbias, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tm_dbias,
+                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using L = B128<BIAS>;
   constexpr int NS = L::kStages;
   // waits poll inline in the variants whose compute loops are short of
@@ -450,23 +451,48 @@ __global__ void __launch_bounds__(448, 1)
       touch32(r1);
       tc_fence_before();
       mbar_arrive(&dq_empty[x]);
-      if ((lt & 31) == 0) bulk_wait_read_all();  // the previous reduces have read the staging tile
-      named_barrier_sync(2, 128);
-      // lane = d, columns = query rows; the staging tile is row-major [MQ][D] fp32
+      if (VARLEN && part == nullptr) {
+        // Packed batches: each warp stages its own 32 columns (its TMEM
+        // lanes) of the step's 64 rows, row-major [64][32] fp32 in its
+        // quarter of the staging area, and reduce-adds them with one tiled
+        // tensor reduce, so the four warps never wait for one another
+        // (0.733 against 0.793 ms on the packed causal batch of mixed
+        // lengths; 4 % slower than the bulk form on the long decoder).
+        const int wq = lt >> 5;
+        const uint32_t qw = qa + wq * (L::kDqBytes / 4);
+        if (lane == 0) bulk_wait_read_all();  // this warp's previous reduce has read its quarter
+        __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        st_shared_f32(qa + (c * 128 + lt) * 4, __uint_as_float(r0[c]));
-        st_shared_f32(qa + ((32 + c) * 128 + lt) * 4, __uint_as_float(r1[c]));
-      }
-      fence_async_smem();
-      named_barrier_sync(2, 128);
-      if ((lt & 31) == 0) {
-        // each warp's first lane reduces a quarter of the tile (16 rows), so
-        // four bulk reduces are in flight at once
-        const int hh = lt >> 5;
-        dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0 + 16 * hh) * 128,
-               smem + L::kDq + hh * (L::kDqBytes / 4), L::kDqBytes / 4);
-        bulk_commit();
+        for (int c = 0; c < 32; ++c) {
+          st_shared_f32(qw + (c * 32 + lane) * 4, __uint_as_float(r0[c]));
+          st_shared_f32(qw + ((32 + c) * 32 + lane) * 4, __uint_as_float(r1[c]));
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_2d(&tm_dq, smem + L::kDq + wq * (L::kDqBytes / 4), 32 * wq,
+                            bh * p.Sq_pad + i0);
+          bulk_commit();
+        }
+      } else {
+        // the whole tile, row-major [MQ][D] fp32; each warp's first lane
+        // reduces (deterministic mode: stores into this key tile's slice) a
+        // quarter of it, 16 rows, so four bulk operations are in flight
+        if ((lt & 31) == 0) bulk_wait_read_all();  // the previous copies have read the tile
+        named_barrier_sync(2, 128);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          st_shared_f32(qa + (c * 128 + lt) * 4, __uint_as_float(r0[c]));
+          st_shared_f32(qa + ((32 + c) * 128 + lt) * 4, __uint_as_float(r1[c]));
+        }
+        fence_async_smem();
+        named_barrier_sync(2, 128);
+        if ((lt & 31) == 0) {
+          const int hh = lt >> 5;
+          dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0 + 16 * hh) * 128,
+                 smem + L::kDq + hh * (L::kDqBytes / 4), L::kDqBytes / 4);
+          bulk_commit();
+        }
       }
     }
     if ((lt & 31) == 0) bulk_wait_all();
@@ -551,7 +577,7 @@ cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.n_kv_tiles) * static_cast<unsigned>(p.B * p.H);
   kern<<<grid, B128<BI>::kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
-                                                   p);
+                                                   m[8], p);
   return cudaGetLastError();
 }
 
