@@ -91,8 +91,10 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 
 /*
  * sdpa_bwd_workspace_size — bytes of device workspace sdpa_bwd needs for
- * this problem size: an fp32 dQ accumulator and two fp32 row vectors, with
- * Sq rounded up to a multiple of 128. Returns 0 for an empty problem.
+ * this problem size: an fp32 dQ accumulator of 128-wide rows (the backward
+ * runs every head dim on 128-wide tiles) and two fp32 row vectors, with Sq
+ * rounded up to a multiple of 128: B*H*ceil128(Sq)*(128 + 2)*4 bytes.
+ * Returns 0 for an empty problem.
  */
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D);
 
@@ -223,7 +225,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
 /*
  * sdpa_bwd_workspace_size_ex — workspace bytes of sdpa_bwd_ex with these
  * options: sdpa_bwd_workspace_size(), or in deterministic mode one fp32 dQ
- * slice per 128-key tile, B*H*ceil128(Sq)*(D*ceil(Sk/128) + 2)*4 bytes.
+ * slice per 128-key tile, B*H*ceil128(Sq)*(128*ceil(Sk/128) + 2)*4 bytes.
  */
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
                                   const sdpa_options* options);
