@@ -346,6 +346,33 @@ def test_minus_infinity_bias_above_the_diagonal_is_the_causal_mask():
         np.testing.assert_allclose(a, b, atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_padded_problem_with_masked_keys_is_the_shorter_problem(causal):
+    """The reading behind the packed-batch tests: a sequence of lq queries
+    and lk keys is the top-left block of a [Mq, Mk] problem whose extra keys
+    get a -inf bias. Its rows of out and lse, its dq rows and its dk, dv rows
+    are those of the [lq, lk] problem, and the padding keys get no gradient
+    (no dropout: the padded problem's counters differ by design)."""
+    H, D, lq, lk, Mq, Mk = 2, 4, 5, 6, 8, 9
+    q, do = rnd((1, H, lq, D), 90), rnd((1, H, lq, D), 91)
+    k, v = rnd((1, H, lk, D), 92), rnd((1, H, lk, D), 93)
+    pad = lambda x, n: np.concatenate([x, np.zeros((1, H, n - x.shape[2], D))], axis=2)
+    qp, dop, kp, vp = pad(q, Mq), pad(do, Mq), pad(k, Mk), pad(v, Mk)
+    bias = np.zeros((1, 1, Mq, Mk))
+    bias[..., lk:] = -np.inf
+    out, lse = oracle.sdpa_fwd(q, k, v, 0.0, causal, None, 0, 0)
+    out_p, lse_p = oracle.sdpa_fwd(qp, kp, vp, 0.0, causal, None, 0, 0, bias=bias)
+    np.testing.assert_allclose(out_p[:, :, :lq], out, atol=1e-14)
+    np.testing.assert_allclose(lse_p[:, :, :lq], lse, atol=1e-14)
+    dq, dk, dv = oracle.sdpa_bwd(do, q, k, v, out, lse, 0.0, causal, 0, 0)
+    dq_p, dk_p, dv_p, _ = oracle.sdpa_bwd(dop, qp, kp, vp, out_p, lse_p, 0.0, causal, 0, 0,
+                                          bias=bias)
+    np.testing.assert_allclose(dq_p[:, :, :lq], dq, atol=1e-13)
+    np.testing.assert_allclose(dk_p[:, :, :lk], dk, atol=1e-13)
+    np.testing.assert_allclose(dv_p[:, :, :lk], dv, atol=1e-13)
+    assert not dk_p[:, :, lk:].any() and not dv_p[:, :, lk:].any()
+
+
 @pytest.mark.parametrize("causal,p", [(False, 0.0), (True, 0.3)])
 def test_bias_gradient_matches_central_differences(causal, p):
     """dbias of L = sum(out * dO), the dropout mask held fixed by (seed, offset)."""
