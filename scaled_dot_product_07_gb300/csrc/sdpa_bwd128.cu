@@ -123,10 +123,18 @@ __global__ void __launch_bounds__(448, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // head-major order (a head's Q and dO stay in L2 while its key tiles run);
-  // low key tiles, which see the most causal query rows, first
-  const int slot = blockIdx.x / p.n_kv_tiles;
-  const int kv_tile = blockIdx.x - slot * p.n_kv_tiles;
+  // Groups of kSlotGroup (batch, head) slots in order (a group's Q and dO
+  // stay in L2 while its key tiles run); within a group key tile j of every
+  // slot before key tile j+1, so the low key tiles, which see the most
+  // causal query rows, go first and the grid ends on short ones.
+  constexpr int kSlotGroup = 8;
+  const int n_slots = p.B * p.H;
+  const int per_group = kSlotGroup * p.n_kv_tiles;
+  const int grp = blockIdx.x / per_group;
+  const int in_grp = blockIdx.x - grp * per_group;
+  const int grp_slots = min(kSlotGroup, n_slots - grp * kSlotGroup);
+  const int kv_tile = in_grp / grp_slots;
+  const int slot = grp * kSlotGroup + (in_grp - kv_tile * grp_slots);
   // batch-major, or head-major when the bias is shared by the batch
   const int b = p.h_major ? slot % p.B : slot / p.H;
   const int h = p.h_major ? slot / p.B : slot - b * p.H;
