@@ -62,7 +62,8 @@ typedef struct {
 typedef enum {
   SDPA_OK = 0,
   SDPA_ERR_INVALID_ARG = 1,    /* shape mismatch, null pointer, p outside [0,1), bad scale */
-  SDPA_ERR_UNSUPPORTED = 2,    /* D not a multiple of 8 in [8, 128], D not innermost */
+  SDPA_ERR_UNSUPPORTED = 2,    /* D not a multiple of 8 in [8, 128], D not innermost, or
+                                  B*H*ceil(max(Sq, Sk)/128) above 2^31-1 (launch grids) */
   SDPA_ERR_ALIGNMENT = 3,      /* base or stride not 16-byte aligned */
   SDPA_ERR_CUDA = 4,           /* a CUDA launch or driver call failed */
   SDPA_ERR_DEVICE_TIMEOUT = 5, /* a kernel gave up on a bounded wait */
@@ -94,7 +95,9 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
  * this problem size: an fp32 dQ accumulator of 128-wide rows (the backward
  * runs every head dim on 128-wide tiles) and two fp32 row vectors, with Sq
  * rounded up to a multiple of 128: B*H*ceil128(Sq)*(128 + 2)*4 bytes.
- * Returns 0 for an empty problem.
+ * Returns 0 for an empty problem, and SIZE_MAX when the size does not fit in
+ * 62 bits (no workspace then satisfies sdpa_bwd, which returns
+ * SDPA_ERR_WORKSPACE).
  */
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D);
 
@@ -225,7 +228,8 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
 /*
  * sdpa_bwd_workspace_size_ex — workspace bytes of sdpa_bwd_ex with these
  * options: sdpa_bwd_workspace_size(), or in deterministic mode one fp32 dQ
- * slice per 128-key tile, B*H*ceil128(Sq)*(128*ceil(Sk/128) + 2)*4 bytes.
+ * slice per 128-key tile, B*H*ceil128(Sq)*(128*ceil(Sk/128) + 2)*4 bytes
+ * (SIZE_MAX when that does not fit in 62 bits).
  */
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
                                   const sdpa_options* options);

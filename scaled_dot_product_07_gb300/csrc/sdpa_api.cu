@@ -1,7 +1,9 @@
 // C-ABI entry points (include/sdpa.h): argument validation, TMA tensor maps
 // for the caller's strided [B,H,S,D] tensors, and kernel launches on the
 // caller's stream. The library allocates no device memory.
+#include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -227,6 +229,15 @@ StridedBf16 strided(const sdpa_tensor* t) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// a*b*c*d fp32 words in bytes (all factors positive), or SIZE_MAX when that
+// does not fit in 62 bits: no workspace satisfies such a request
+size_t checked_bytes(int64_t a, int64_t b, int64_t c, int64_t d) {
+  if (static_cast<double>(a) * static_cast<double>(b) * static_cast<double>(c) *
+          static_cast<double>(d) * 4.0 >= 4.6e18)
+    return SIZE_MAX;
+  return static_cast<size_t>(a * b * c * d * 4);
+}
+
 // Head dims served: multiples of 8 up to 128. The kernels are built for 64
 // and 128; a smaller D runs the next larger one, with the missing columns of
 // q, k, v, dout read as zeros by the TMA loads (out-of-bounds fill) and never
@@ -290,6 +301,18 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
                             Opts* r) {
   Opts x;
   x.H_total = static_cast<int>(H);
+  // the launch grids number the 128-row query and key tiles of every (batch,
+  // head) in int (sizes of real tensors stay far below this; views with
+  // overlapping strides need not)
+  const double tiles = static_cast<double>(B) * static_cast<double>(H) *
+                       static_cast<double>((std::max(Sq, Sk) + 127) / 128);
+  if (tiles > 2147483647.0) return SDPA_ERR_UNSUPPORTED;
+  // the global counter ((b*H_total + h)*Sq + i)*Sk + j must fit in 64 bits
+  auto counter_fits = [&](int64_t b_end, int64_t h_total) {
+    return static_cast<double>(b_end) * static_cast<double>(h_total) * static_cast<double>(Sq) *
+               static_cast<double>(Sk) < 1.8e19;
+  };
+  if (!counter_fits(B, H)) return SDPA_ERR_INVALID_ARG;
   if (o) {
     if (o->batch_offset < 0 || o->head_offset < 0 || o->total_heads < 0)
       return SDPA_ERR_INVALID_ARG;
@@ -298,10 +321,7 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
     if (o->head_offset + H > Ht) return SDPA_ERR_INVALID_ARG;
     const int64_t kMaxInt = 0x7fffffff;
     if (o->batch_offset + B > kMaxInt || Ht > kMaxInt) return SDPA_ERR_INVALID_ARG;
-    // the global counter ((b*H_total + h)*Sq + i)*Sk + j must fit in 64 bits
-    const double n_max = static_cast<double>(o->batch_offset + B) * static_cast<double>(Ht) *
-                         static_cast<double>(Sq) * static_cast<double>(Sk);
-    if (n_max >= 1.8e19) return SDPA_ERR_INVALID_ARG;
+    if (!counter_fits(o->batch_offset + B, Ht)) return SDPA_ERR_INVALID_ARG;
     if (o->attn_bias) {
       const sdpa_status s = check_bias(o->attn_bias, B, H, Sq, Sk, &x.bias);
       if (s != SDPA_OK) return s;
@@ -595,17 +615,14 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D) {
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
-  const int64_t Sq_pad = round_up(Sq, 128);
-  return static_cast<size_t>(B * H * Sq_pad * (kBwdHeadDim + 2) * 4);
+  return checked_bytes(B, H, round_up(Sq, 128), kBwdHeadDim + 2);
 }
 
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
                                   const sdpa_options* options) {
   if (!options || !options->deterministic) return sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
-  const int64_t Sq_pad = round_up(Sq, 128);
-  const int64_t n_kv = (Sk + 127) / 128;
-  return static_cast<size_t>(B * H * Sq_pad * (kBwdHeadDim * n_kv + 2) * 4);
+  return checked_bytes(B, H, round_up(Sq, 128), kBwdHeadDim * ((Sk + 127) / 128) + 2);
 }
 
 sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,

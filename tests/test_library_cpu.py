@@ -67,6 +67,16 @@ def test_workspace_size(lib):
 FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced
 
 
+def test_workspace_size_saturates_instead_of_wrapping(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    size_max = 2**64 - 1
+    # 2^62 fp32 rows would wrap a 64-bit byte count; no workspace satisfies it
+    assert sdpa.sdpa_bwd_workspace_size(2**30, 2**20, 2**20, 1, 128) == size_max
+    assert sdpa.sdpa_bwd_workspace_size_ex(2**10, 2**10, 2**20, 2**30, 128, True) == size_max
+    # the largest sizes below the limit are exact
+    assert sdpa.sdpa_bwd_workspace_size(2**20, 2**10, 2**12, 1, 128) == 2**42 * 130 * 4
+
+
 def desc(B, H, S, D, layout="BHSE", data=FAKE, stride=None):
     import scaled_dot_product_07_gb300 as sdpa
     t = sdpa.SdpaTensor()
@@ -115,6 +125,21 @@ def test_forward_argument_errors(lib):
     assert fwd_status(lib, ok(), ok(), ok(), ok(), lse=FAKE + 2) == 1
     # a key length of zero with queries present
     assert fwd_status(lib, ok(), desc(B, H, 0, D), desc(B, H, 0, D), ok()) == 1
+
+
+def test_launch_grid_and_counter_limits(lib):
+    # views with overlapping strides can describe problems whose grids of
+    # 128-row tiles do not fit in int, or whose dropout counter does not fit
+    # in 64 bits; both are refused on the host
+    D = 64
+    small = (D, D, D, 1)
+    big = desc(2**15, 2**15, 2**20, D, stride=small)        # 2^43 query tiles
+    assert fwd_status(lib, big, big, big, big) == 2
+    wide = desc(2**7, 1, 2**30, D, stride=small)            # 2^30 tiles, counter 2^67
+    assert fwd_status(lib, wide, wide, wide, wide) == 1
+    r = ctypes.byref
+    assert lib.sdpa_bwd(r(big), r(big), r(big), r(big), r(big), ctypes.c_void_p(FAKE), 0.0, 0, 0,
+                        0, 0.125, r(big), r(big), r(big), ctypes.c_void_p(FAKE), 2**40, None) == 2
 
 
 def test_empty_problems_are_no_ops(lib):
