@@ -208,6 +208,14 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  *     the tiles finish). It needs the larger workspace that
  *     sdpa_bwd_workspace_size_ex() reports and moves about twice the partials'
  *     bytes through HBM.
+ *   kernel_events: NULL, or a pointer to two cudaEvent_t handles that the
+ *     call records on `stream` immediately before and after its main kernel:
+ *     the forward kernel, or the backward's main kernel (between its
+ *     preprocess and its dQ kernel). A caller times that kernel alone with
+ *     cudaEventElapsedTime, without the host work of the call or the
+ *     backward's small kernels. Both handles must be non-NULL. Recording is
+ *     stream-ordered and allowed during stream capture. A call that launches
+ *     no main kernel (an empty problem) records neither event.
  */
 typedef struct {
   const uint64_t* rng_state;
@@ -217,6 +225,7 @@ typedef struct {
   int deterministic;
   const sdpa_tensor* attn_bias;
   sdpa_tensor* dbias;
+  void* const* kernel_events;
 } sdpa_options;
 
 /* sdpa_fwd with options (NULL options = sdpa_fwd). */

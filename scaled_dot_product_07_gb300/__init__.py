@@ -76,7 +76,7 @@ class SdpaOptions(ctypes.Structure):
     _fields_ = [("rng_state", ctypes.c_void_p), ("batch_offset", ctypes.c_int64),
                 ("head_offset", ctypes.c_int64), ("total_heads", ctypes.c_int64),
                 ("deterministic", ctypes.c_int), ("attn_bias", ctypes.c_void_p),
-                ("dbias", ctypes.c_void_p)]
+                ("dbias", ctypes.c_void_p), ("kernel_events", ctypes.c_void_p)]
 
 
 def library_path():
@@ -285,13 +285,29 @@ def _bias_desc(t, name):
     return d
 
 
+def _event_handle(e):
+    """The cudaEvent_t of a torch.cuda.Event (created by its first record)."""
+    h = int(getattr(e, "cuda_event", 0) or 0)
+    if h == 0:
+        raise ValueError("kernel_events: record each torch.cuda.Event once before passing it "
+                         "(torch creates the CUDA event on its first record)")
+    return h
+
+
 def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deterministic=False,
-             attn_bias=None, dbias=None):
+             attn_bias=None, dbias=None, kernel_events=None):
     """sdpa_options (by pointer) for the *_ex calls; rng_state is a device
     tensor holding {seed, offset} as two 64-bit integers, or None; attn_bias
-    and dbias are bfloat16 tensors or None."""
+    and dbias are bfloat16 tensors or None; kernel_events is None or a pair of
+    torch.cuda.Event (timing enabled, each recorded once already) that the
+    library records around the call's main kernel."""
     o = SdpaOptions()
     o._keep = []
+    if kernel_events is not None:
+        a, b = kernel_events
+        handles = (ctypes.c_void_p * 2)(_event_handle(a), _event_handle(b))
+        o._keep.append(handles)
+        o.kernel_events = ctypes.addressof(handles)
     if attn_bias is not None:
         bd = _bias_desc(attn_bias, "attn_bias")
         o._keep.append(bd)
@@ -313,12 +329,13 @@ def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deter
 
 def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset=0,
                 rng_state=None, batch_offset=0, head_offset=0, total_heads=0, attn_bias=None,
-                out=None, lse=None):
+                out=None, lse=None, kernel_events=None):
     """Forward with options: ``rng_state`` (device {seed, offset}, read by the
     kernels when they run, e.g. inside a replayed CUDA graph), the batch /
-    head position of this call in a larger split problem, and an additive
-    bfloat16 ``attn_bias`` [B or 1, H or 1, Sq, Sk] of the scaled scores.
-    Returns (out, lse)."""
+    head position of this call in a larger split problem, an additive
+    bfloat16 ``attn_bias`` [B or 1, H or 1, Sq, Sk] of the scaled scores, and
+    ``kernel_events`` (a pair of torch.cuda.Event recorded around the forward
+    kernel, for timing it alone). Returns (out, lse)."""
     import torch
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -326,7 +343,8 @@ def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, off
     B, H, Sq, D = q.shape
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
-    opt = _options(rng_state, batch_offset, head_offset, total_heads, attn_bias=attn_bias)
+    opt = _options(rng_state, batch_offset, head_offset, total_heads, attn_bias=attn_bias,
+                   kernel_events=kernel_events)
     dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.sdpa_fwd_ex(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), float(dropout_p),
                          int(bool(is_causal)), _default_scale(D, scale), int(seed), int(offset),
@@ -344,10 +362,11 @@ def sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, deterministic=False):
 def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
                 scale=None, rng_state=None, batch_offset=0, head_offset=0, total_heads=0,
                 deterministic=False, attn_bias=None, dbias=None, dq=None, dk=None, dv=None,
-                workspace=None):
+                workspace=None, kernel_events=None):
     """Backward with options (see :func:`sdpa_fwd_ex`); ``deterministic``
     selects the fixed-order dQ accumulation. ``dbias``: None, True (allocate)
     or a bfloat16 [B, H, Sq, Sk] tensor that receives the bias gradient dS.
+    ``kernel_events`` are recorded around the backward's main kernel.
     Returns (dq, dk, dv), or (dq, dk, dv, dbias) when dbias is requested."""
     import torch
     lib = load_library()
@@ -363,7 +382,7 @@ def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0,
         pad = (Sk + 7) // 8 * 8
         dbias = torch.empty((B, H, Sq, pad), dtype=torch.bfloat16, device=q.device)[..., :Sk]
     opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic, attn_bias,
-                   dbias)
+                   dbias, kernel_events)
     need = int(lib.sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

@@ -260,7 +260,13 @@ struct Opts {
   AttnBias bias{nullptr, 0, 0, 0};
   int64_t bias_B = 0, bias_H = 0;  // the bias's own batch and head extents (1 when shared)
   DBias dbias{nullptr, 0, 0, 0};
+  cudaEvent_t ev_begin = nullptr, ev_end = nullptr;  // around the main kernel
 };
+
+// Records one of the caller's kernel events (none when it is null).
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+  return ev ? cudaEventRecord(ev, stream) : cudaSuccess;
+}
 
 sdpa_status check_bias(const sdpa_tensor* t, int64_t B, int64_t H, int64_t Sq, int64_t Sk,
                        AttnBias* out) {
@@ -332,6 +338,11 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
       if (!o->attn_bias) return SDPA_ERR_INVALID_ARG;
       const sdpa_status s = check_dbias(o->dbias, B, H, Sq, Sk, &x.dbias);
       if (s != SDPA_OK) return s;
+    }
+    if (o->kernel_events) {
+      x.ev_begin = static_cast<cudaEvent_t>(o->kernel_events[0]);
+      x.ev_end = static_cast<cudaEvent_t>(o->kernel_events[1]);
+      if (!x.ev_begin || !x.ev_end) return SDPA_ERR_INVALID_ARG;
     }
     x.rng = o->rng_state;
     x.b0 = static_cast<int>(o->batch_offset);
@@ -409,7 +420,10 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return SDPA_ERR_CUDA;
   const bool dropout = dropout_p > 0.0;
-  return finish(launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream), stream);
+  cudaError_t e = record_event(opt.ev_begin, stream);
+  if (e == cudaSuccess) e = launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream);
+  if (e == cudaSuccess) e = record_event(opt.ev_end, stream);
+  return finish(e, stream);
 }
 
 // Shared tail of the backward entry points: workspace, tensor maps, the
@@ -515,7 +529,10 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
                                  static_cast<int>(Sq), static_cast<int>(Sk), stream);
     if (e != cudaSuccess) return SDPA_ERR_CUDA;
   }
-  e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
+  e = record_event(opt.ev_begin, stream);
+  if (e == cudaSuccess)
+    e = launch_bwd_main(static_cast<int>(Dk), is_causal != 0, dropout_p > 0.0, maps, p, stream);
+  if (e == cudaSuccess) e = record_event(opt.ev_end, stream);
   if (e != cudaSuccess) return SDPA_ERR_CUDA;
 
   if (opt.det) {

@@ -232,6 +232,9 @@ def test_option_errors_are_reported_before_any_launch(lib):
     assert fwd(options(batch_offset=-1)) == 1
     assert fwd(options(total_heads=-2)) == 1
     assert fwd(options(rng_state=FAKE + 4)) == 3
+    # kernel events need both handles (checked before anything is recorded)
+    handles = (ctypes.c_void_p * 2)(FAKE, None)
+    assert fwd(options(kernel_events=ctypes.addressof(handles))) == 1
     # the global counter must fit in 64 bits
     assert fwd(options(batch_offset=2**30, total_heads=2**30)) == 1
 

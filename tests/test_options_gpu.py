@@ -11,7 +11,9 @@
   whole problem's heads with their global indices (the head split of
   test_sdpa_loop_split, "DID loop split for SDPA", NVIDIA/Fuser PR 3711);
 - deterministic backward: dq, dk, dv are bitwise identical across runs and
-  within the parity bounds of the oracle.
+  within the parity bounds of the oracle;
+- kernel events: the pair the caller passes is recorded around the forward
+  kernel and around the backward's main kernel, without changing results.
 """
 
 import numpy as np
@@ -141,3 +143,38 @@ def test_deterministic_backward_is_reproducible_and_matches_the_oracle(cuda_lib,
     dq_a, _, _ = cuda_lib.sdpa_bwd(do, q, k, v, out, lse, p, causal, w.seed, w.offset)
     a, b = to_np(dq_a), to_np(runs[0][0])
     assert np.linalg.norm(a - b) <= 1e-2 * max(np.linalg.norm(b), 1e-30)
+
+
+def test_kernel_events_bracket_the_main_kernels(cuda_lib):
+    """kernel_events: the library records the pair around the forward kernel
+    and around the backward's main kernel; the results are those of the plain
+    calls, and each bracketed time is positive and inside its whole call."""
+    sdpa = cuda_lib
+    B, H, S, D, p = 2, 4, 1024, 128, 0.1
+    q, k, v, do = (x.cuda() for x in _inputs(B, H, S, S, D, 77))
+    out0, lse0, _, _ = sdpa.sdpa_fwd(q, k, v, p, True, None, 5, 8)
+    dq0, dk0, dv0 = sdpa.sdpa_bwd(do, q, k, v, out0, lse0, p, True, 5, 8)
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    for e in ev:
+        e.record(st)  # creates the CUDA events
+    ev[0].record(st)
+    out, lse = sdpa.sdpa_fwd_ex(q, k, v, p, True, None, 5, 8, kernel_events=(ev[1], ev[2]))
+    ev[3].record(st)
+    ev[4].record(st)
+    dq, dk, dv = sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, p, True, 5, 8,
+                                  kernel_events=(ev[5], ev[6]))
+    ev[7].record(st)
+    torch.cuda.synchronize()
+    assert sdpa.sdpa_check_device() == 0
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
+    assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+    a, b = to_np(dq), to_np(dq0)
+    assert np.linalg.norm(a - b) <= 1e-2 * max(np.linalg.norm(b), 1e-30)
+    fwd_k, fwd_all = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    bwd_k, bwd_all = ev[5].elapsed_time(ev[6]), ev[4].elapsed_time(ev[7])
+    assert 0.0 < fwd_k <= fwd_all
+    assert 0.0 < bwd_k < bwd_all  # the backward's preprocess and dQ kernels are outside
+    with pytest.raises(ValueError):
+        sdpa.sdpa_fwd_ex(q, k, v, p, True, kernel_events=(torch.cuda.Event(enable_timing=True),
+                                                          ev[2]))
