@@ -190,18 +190,5 @@ cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStre
 // backward never visits for row i.
 cudaError_t launch_dbias_zero_causal(const DBias& t, int B, int H, int Sq, int Sk,
                                      cudaStream_t stream);
-cudaError_t launch_dropout_mask(int64_t B, int64_t H, int64_t Sq, int64_t Sk, uint32_t threshold,
-                                PhiloxKey pk, uint8_t* mask, cudaStream_t stream);
-cudaError_t launch_selftest_wait(uint32_t* err, uint64_t limit_ns, cudaStream_t stream);
-
-// Dynamic shared memory sizes (for validation against the device limit).
-size_t fwd_smem_bytes(int D);
-size_t bwd_smem_bytes(int D);
-size_t bwd_d128_smem_bytes();
-
-__host__ __device__ inline uint8_t* align_up_1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023u) &
-                                    ~static_cast<uintptr_t>(1023u));
-}
 
 }  // namespace sdpa

@@ -191,11 +191,6 @@ unsigned elementwise_grid(int64_t work_items) {
 
 }  // namespace
 
-size_t bwd_smem_bytes(int D) {
-  (void)D;
-  return bwd_d128_smem_bytes();
-}
-
 cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream) {
   const int64_t threads = static_cast<int64_t>(p.B) * p.H * p.Sq_pad * (p.D / 8);
   bwd_preprocess_kernel<<<elementwise_grid(threads), 256, 0, stream>>>(p);

@@ -591,8 +591,6 @@ cudaError_t launch_t(const CUtensorMap* m, const BwdParams& p, cudaStream_t stre
 
 }  // namespace
 
-size_t bwd_d128_smem_bytes() { return B128<false>::kAlloc; }
-
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout, const CUtensorMap* maps,
                                  const BwdParams& p, cudaStream_t stream) {
   if (p.cu_q != nullptr) {  // packed batch (no bias)

@@ -75,6 +75,7 @@ struct FwdLayout {
   __host__ __device__ static constexpr uint32_t tmem_o(int i) { return 256u + D * i; }
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kThreads = 320;
+  static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ void reg_touch(uint32_t (&r)[32]) {
@@ -970,10 +971,6 @@ cudaError_t launch_fwd_bias_t(const CUtensorMap* maps, const FwdParams& p, cudaS
 }
 
 }  // namespace
-
-size_t fwd_smem_bytes(int D) {
-  return D == 64 ? FwdLayout<64>::kAlloc : FwdLayout<128>::kAlloc;
-}
 
 cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps,
                        const FwdParams& p, cudaStream_t stream) {
