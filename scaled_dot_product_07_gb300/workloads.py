@@ -104,16 +104,6 @@ def to_layout(x, layout):
     raise ValueError(f"unknown layout {layout}")
 
 
-def empty_like_layout(shape, layout, dtype, device):
-    """Uninitialised logical-[B,H,S,D] tensor with the layout's strides."""
-    B, H, S, D = shape
-    if layout == "BHSE":
-        return torch.empty((B, H, S, D), dtype=dtype, device=device)
-    if layout == "BSHE":
-        return torch.empty((B, S, H, D), dtype=dtype, device=device).permute(0, 2, 1, 3)
-    raise ValueError(f"unknown layout {layout}")
-
-
 def draw_bias(shape, seed, kind="random"):
     """Seeded bfloat16 additive-bias input of logical shape [Bb, Hb, Sq, Sk]
     (CPU, contiguous).

@@ -8,7 +8,6 @@ and the max over ranks of the timed region, which is what this checks.
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

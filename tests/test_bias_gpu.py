@@ -14,7 +14,7 @@ import torch
 
 from scaled_dot_product_07_gb300 import workloads as W
 
-from test_parity_gpu import compare, oracle_heads, rel_l2, to_np  # noqa: F401
+from test_parity_gpu import compare, rel_l2, to_np
 
 import oracle
 
