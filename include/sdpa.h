@@ -214,8 +214,9 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  *     preprocess and its dQ kernel). A caller times that kernel alone with
  *     cudaEventElapsedTime, without the host work of the call or the
  *     backward's small kernels. Both handles must be non-NULL. Recording is
- *     stream-ordered and allowed during stream capture. A call that launches
- *     no main kernel (an empty problem) records neither event.
+ *     stream-ordered (under stream capture the records become event-record
+ *     nodes of the graph). A call that launches no main kernel (an empty
+ *     problem) records neither event.
  */
 typedef struct {
   const uint64_t* rng_state;
