@@ -59,6 +59,21 @@ def flops(w):
     return 4 * p, 10 * p
 
 
+def bwd_small_kernel_bytes(w):
+    """Algorithmic HBM bytes of the backward's two small kernels per call.
+
+    bwd_preprocess_kernel reads out and dout (bf16) and lse (fp32), and writes
+    the padded lse*log2(e) and Delta rows and the zeroed fp32 dQ accumulator
+    (rows of 128 columns, Sq padded to 128); bwd_dq_convert_kernel reads the
+    caller's D columns of the accumulator's real rows and writes dq (bf16).
+    """
+    bh = w.B * w.H
+    sq_pad = (w.Sq + 127) // 128 * 128
+    pre = bh * (2 * w.Sq * w.D * 2 + 4 * w.Sq + sq_pad * (128 + 2) * 4)
+    conv = bh * (w.Sq * w.D * 4 + w.Sq * w.D * 2)
+    return pre + conv
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -356,6 +371,10 @@ def bench_ours(args, w):
     # every flop of each pass is in its main kernel
     fwd_kernel_tf = f_fwd / (fwd_kernel_ms * 1e-3) / 1e12
     bwd_main_tf = f_bwd / (bwd_main_ms * 1e-3) / 1e12
+    # the backward call's two HBM-bound kernels: the call's time less its main
+    # kernel's (launch gaps included, so a lower bound on their rate)
+    small_ms = max(bwd_ms - bwd_main_ms, 1e-6)
+    small_gbs = bwd_small_kernel_bytes(w) / (small_ms * 1e-3) / 1e9
     pk, pk_src = peaks()
     peak = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
 
@@ -593,6 +612,14 @@ def bench_ours(args, w):
                      "timing": "CUDA events recorded by the library around each launch "
                                "(kernel_events), mean over the timed steps",
                      "peak_source": f"{pk_src} bf16_tflops (burst)"},
+        "roofline_bwd_hbm": {"kernel": "bwd_preprocess_kernel + bwd_dq_convert_kernel",
+                             "bound": "hbm", "achieved": small_gbs,
+                             "peak": pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]), "unit": "GB/s",
+                             "frac": small_gbs / pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+                             "bytes": bwd_small_kernel_bytes(w), "ms_per_call": small_ms,
+                             "timing": "backward call events less the main kernel's events "
+                                       "(launch gaps included)",
+                             "peak_source": f"{pk_src} hbm_gbs"},
         "roofline_fwd": {"kernel": "fwd_kernel", "bound": "tensor", "achieved": fwd_kernel_tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": fwd_kernel_tf / peak,
                          "traffic": kernel_traffic("fwd_kernel"), "ms_per_launch": fwd_kernel_ms,

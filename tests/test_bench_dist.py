@@ -57,3 +57,24 @@ def test_flop_count_matches_the_pair_formula():
     # causal with more queries than keys: rows past Sk see every key
     w2 = W.make_workload("tiny", Sq=10, Sk=4)
     assert bench.pairs(w2) == sum(min(i + 1, 4) for i in range(10))
+
+
+def test_small_kernel_bytes_of_the_backward():
+    """Bytes behind the HBM roofline of the backward's preprocess and dQ
+    conversion: at B8 H16 S4096 D128, 0.543 GB (out, dout read; lse read;
+    lse2, Delta and the zeroed 128-column fp32 accumulator written) plus
+    0.403 GB (accumulator read, dq written)."""
+    import bench
+    from scaled_dot_product_07_gb300 import workloads as W
+    w = W.WORKLOADS["decoder_long"]
+    heads, rows = 8 * 16, 4096
+    out_dout = 2 * rows * 128 * 2          # bf16 rows of out and dout
+    written = rows * (128 + 2) * 4         # accumulator zeros, lse2, Delta
+    convert = rows * 128 * 4 + rows * 128 * 2
+    assert bench.bwd_small_kernel_bytes(w) == heads * (out_dout + 4 * rows + written + convert)
+    # a smaller head dim reads and writes only its own columns, but the
+    # accumulator rows stay 128 wide; Sq is padded to 128 for the written rows
+    w64 = W.make_workload("tiny", Sq=200, D=64)
+    pad = 256
+    per_head = 2 * 200 * 64 * 2 + 4 * 200 + pad * 130 * 4 + 200 * 64 * 6
+    assert bench.bwd_small_kernel_bytes(w64) == w64.B * w64.H * per_head
