@@ -74,10 +74,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Device address of g_wait_error on the current device (looked up once per
+// device under a lock, with that device current). nullptr on failure.
 uint32_t* error_word() {
   static uint32_t* ptrs[64] = {nullptr};
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!ptrs[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_wait_error) != cudaSuccess) return nullptr;

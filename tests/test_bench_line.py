@@ -1,0 +1,93 @@
+"""The bench's JSON line, assembled on CPU from fake measurements.
+
+The line is built by one pure function (bench.assemble_line); these tests
+give it made-up timings, clock samples and extended-block entries and check
+that every key of the bench contract comes out, with the arithmetic the
+docstrings state, and that the line is valid JSON.
+"""
+
+import json
+
+import bench
+from scaled_dot_product_07_gb300 import workloads as W
+
+PEAKS = {"hbm_gbs": 6683.2, "bf16_tflops": 1940.8, "bf16_tflops_sustained": 1728.1}
+
+
+def _timings(steps=20):
+    return {"total_ms": 1.8 * steps, "fwd_ms": 0.41, "bwd_ms": 1.36, "fwd_kernel_ms": 0.405,
+            "bwd_main_ms": 1.20}
+
+
+def test_line_has_every_contract_key():
+    w = W.WORKLOADS["decoder_long"]
+    clocks = bench.summarize_clocks([(0.0, 1900.0, 2070.0, 900.0, set()),
+                                     (0.1, 1950.0, 2070.0, 950.0, {"sw_power_cap"})], "nvml")
+    sustained = {"steps": 1600, "ms_per_step": 1.85, "tflops": 1040.0, "clocks": clocks}
+    extras = {"graph_step": {"ms": 1.7}}
+    e2e = {"value": 590.0, "unit": "TFLOP/s", "h2d_bytes_per_step": 4, "d2h_bytes_per_step": 8,
+           "copies_declared": True}
+    cpu = {"value": 0.034, "unit": "TFLOP/s", "cores": 16, "kind": "oracle", "sample": "x"}
+    line = bench.assemble_line(w, 1, 20, 5, _timings(), PEAKS, "measured", clocks, sustained,
+                               extras, e2e, cpu)
+    json.loads(json.dumps(line))
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks", "cpu_baseline", "sustained",
+                "extended", "roofline_fwd", "roofline_bwd_hbm"):
+        assert key in line, key
+    assert line["metric"] == bench.METRIC
+    assert line["dtype"] == "bf16" and line["unit"] == "TFLOP/s"
+    assert line["config"]["workload"].startswith("decoder_long B8 H16 Sq4096 Sk4096 D128 causal")
+    f, b = bench.flops(w)
+    assert abs(line["value"] - (f + b) / 1.8e-3 / 1e12) < 1e-9
+    r = line["roofline"]
+    for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert key in r
+    assert r["bound"] == "tensor" and r["peak"] == PEAKS["bf16_tflops"]
+    assert abs(r["achieved"] - b / 1.2e-3 / 1e12) < 1e-9
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    assert line["sustained"]["peak"] == PEAKS["bf16_tflops_sustained"]
+    assert abs(line["sustained"]["frac"] - 1040.0 / 1728.1) < 1e-12
+    hbm = line["roofline_bwd_hbm"]
+    assert hbm["achieved"] > 0 and hbm["peak"] == PEAKS["hbm_gbs"]
+    assert line["gpu_launches"] == 4 * 20
+    assert line["cpu_baseline"]["cores"] == 16
+
+
+def test_hbm_figure_is_null_when_the_difference_is_not_positive():
+    w = W.WORKLOADS["decoder_long"]
+    t = _timings()
+    t["bwd_main_ms"] = t["bwd_ms"] + 0.001  # event noise
+    line = bench.assemble_line(w, 1, 20, 5, t, PEAKS, "measured",
+                               bench.summarize_clocks([], "nvml"))
+    assert line["roofline_bwd_hbm"]["achieved"] is None
+    assert line["roofline_bwd_hbm"]["frac"] is None
+    json.dumps(line)
+
+
+def test_fallback_peaks_are_used_without_the_measured_file():
+    w = W.WORKLOADS["decoder_long"]
+    line = bench.assemble_line(w, 2, 10, 3, _timings(10), bench.FALLBACK_PEAKS, "fallback",
+                               bench.summarize_clocks([], None))
+    assert line["roofline"]["peak"] == bench.FALLBACK_PEAKS["bf16_tflops"]
+    assert "fallback" in line["roofline"]["peak_source"]
+    # weak scaling: two ranks, each with the whole workload
+    f, b = bench.flops(w)
+    assert abs(line["value"] - 2 * (f + b) / 1.8e-3 / 1e12) < 1e-9
+    assert line["clocks"]["reasons"] == ["no clock source"]
+
+
+def test_clock_window_keeps_only_its_samples_and_flags_throttling():
+    s = bench.ClockSampler(0)
+    s.source = "nvml"
+    s.samples = [(0.5, 2070.0, 2070.0, 200.0, set()),
+                 (1.0, 1800.0, 2070.0, 1000.0, {"sw_power_cap"}),
+                 (1.5, 1700.0, 2070.0, 1100.0, {"sw_power_cap"}),
+                 (2.5, 1000.0, 2070.0, 1100.0, {"hw_slowdown"})]
+    c = s.window(0.9, 2.0)
+    assert c["samples_under_load"] == 2
+    assert c["sm_mhz"] == 1750.0 and c["sm_min_mhz"] == 1700.0
+    assert c["reasons"] == ["sw_power_cap"] and c["rejected"] is False
+    c2 = s.window(0.9, 3.0)
+    assert c2["rejected"] is True and "hw_slowdown" in c2["reasons"]

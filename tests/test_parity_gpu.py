@@ -63,14 +63,30 @@ def compare(gpu, ref, heads, tag):
         assert e <= GRAD_RTOL_L2, msg
 
 
+def spread_heads(w, n):
+    """n heads spread over the whole grid: one head in each of n equal groups
+    of consecutive (b, h), at a different position inside each group. At the
+    long decoder shape (128 heads, n = 16) these are the heads 8g + g % 8:
+    every 8-head group of the backward's CTA order, and in the two-item
+    forward the first items of CTAs 0-15 (head 0), the middle CTAs (heads
+    27, 36) and the last CTAs (head 63), and the second items of CTAs
+    1008-1023 (head 64) and 0-15 (head 127)."""
+    bh_total = w.B * w.H
+    g = bh_total // n
+    picks = sorted({min(bh_total - 1, i * g + (i % g)) for i in range(n)} | {bh_total - 1})
+    return [divmod(bh, w.H) for bh in picks]
+
+
 def sampled_heads(w):
     if w.B * w.H <= 24:
         return [(b, h) for b in range(w.B) for h in range(w.H)]
+    if w.Sq * w.Sk >= 1 << 24:   # the long decoder: 16 heads across the grid
+        return spread_heads(w, 16)
+    if w.Sq * w.Sk >= 1 << 23:   # cross-attention: 8 heads across the grid
+        return spread_heads(w, 8)
     cand = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 3), (w.B // 3, w.H - 2)]
     if w.Sq * w.Sk <= 1 << 20:
         cand += [(1, 5), (w.B - 2, 1), (w.B // 4, w.H // 2), (w.B - 1, 0)]
-    if w.Sq * w.Sk >= 1 << 24:
-        cand = cand[:2]
     return sorted(set(cand))
 
 
@@ -155,26 +171,51 @@ def _block_select_inputs(Sq, Sk, D, j0, i0):
     return tuple(x.to(torch.bfloat16) for x in (q, k, v, do))
 
 
+def expected_kept_pattern(keep, Sq, Sk, D, j0, i0, causal):
+    """Which out[i, e] and dV[j0+e', e] are non-zero for the block-select
+    inputs: the element is kept and (causal) key j0+e is visible from row i."""
+    vis = np.ones((Sq, Sk), dtype=bool)
+    if causal:
+        vis = np.arange(Sk)[None, :] <= np.arange(Sq)[:, None]
+    live = keep & vis
+    rows = min(D, Sq - i0)
+    return live[:, j0:j0 + D], live[i0:i0 + rows, j0:j0 + D].T, rows
+
+
 # key counts that are multiples of 4 take the backward's quad-shared mask
-# draws, the others its per-element draws
-@pytest.mark.parametrize("D,Sq,Sk,j0,i0", [(64, 256, 300, 100, 150), (128, 300, 520, 260, 40),
-                                           (64, 256, 301, 98, 150), (128, 300, 523, 262, 40)])
-def test_kernel_masks_match_oracle_bit_exact(cuda_lib, D, Sq, Sk, j0, i0):
+# draws, the others its per-element draws; the causal cases put the block on
+# the diagonal tiles of both kernels (rows and keys straddle 128-row tiles),
+# where masking and dropout meet
+@pytest.mark.parametrize("D,Sq,Sk,j0,i0,causal", [
+    (64, 256, 300, 100, 150, False), (128, 300, 520, 260, 40, False),
+    (64, 256, 301, 98, 150, False), (128, 300, 523, 262, 40, False),
+    (64, 300, 300, 100, 100, True), (128, 400, 400, 100, 90, True),
+    (64, 320, 301, 98, 110, True), (128, 300, 523, 130, 150, True),
+    (64, 520, 520, 250, 240, True)])
+def test_kernel_masks_match_oracle_bit_exact(cuda_lib, D, Sq, Sk, j0, i0, causal):
     """The forward and backward kernels drop exactly the oracle's elements.
 
-    out[i, e] = P~[i, j0+e] (non-zero iff kept) and dV[j0+e', e] =
-    P~[i0+e, j0+e'] expose the masks the kernels generated inside their tiles.
+    out[i, e] = P~[i, j0+e] (non-zero iff kept and visible) and dV[j0+e', e] =
+    P~[i0+e, j0+e'] expose the masks the kernels generated inside their
+    tiles. The expected pattern is first confirmed on the oracle's own
+    output for the same inputs.
     """
     p, seed, offset = 0.4, 31337, 12345
-    q, k, v, do = (x.cuda() for x in _block_select_inputs(Sq, Sk, D, j0, i0))
-    out, lse, _, _ = cuda_lib.sdpa_fwd(q, k, v, p, False, None, seed, offset)
-    dq, dk, dv = cuda_lib.sdpa_bwd(do, q, k, v, out, lse, p, False, seed, offset)
+    inputs = _block_select_inputs(Sq, Sk, D, j0, i0)
     keep = oracle.keep_mask(1, 1, Sq, Sk, p, seed, offset)[0, 0]
-    fwd_kept = out[0, 0].float().cpu().numpy() != 0
-    assert np.array_equal(fwd_kept, keep[:, j0:j0 + D])
-    rows = min(D, Sq - i0)
-    bwd_kept = dv[0, 0, j0:j0 + D, :rows].float().cpu().numpy() != 0
-    assert np.array_equal(bwd_kept, keep[i0:i0 + rows, j0:j0 + D].T)
+    want_fwd, want_bwd, rows = expected_kept_pattern(keep, Sq, Sk, D, j0, i0, causal)
+    f64 = [x.float().numpy().astype(np.float64) for x in inputs]
+    ro, rl = oracle.sdpa_fwd(f64[0], f64[1], f64[2], p, causal, None, seed, offset)
+    _, _, rdv = oracle.sdpa_bwd(f64[3], f64[0], f64[1], f64[2], ro, rl, p, causal, seed, offset)
+    assert np.array_equal(ro[0, 0] != 0, want_fwd)
+    assert np.array_equal(rdv[0, 0, j0:j0 + D, :rows] != 0, want_bwd)
+    q, k, v, do = (x.cuda() for x in inputs)
+    out, lse, _, _ = cuda_lib.sdpa_fwd(q, k, v, p, causal, None, seed, offset)
+    dq, dk, dv = cuda_lib.sdpa_bwd(do, q, k, v, out, lse, p, causal, seed, offset)
+    torch.cuda.synchronize()
+    assert cuda_lib.sdpa_check_device() == 0
+    assert np.array_equal(out[0, 0].float().cpu().numpy() != 0, want_fwd)
+    assert np.array_equal(dv[0, 0, j0:j0 + D, :rows].float().cpu().numpy() != 0, want_bwd)
 
 
 def test_empty_and_degenerate(cuda_lib):
