@@ -176,6 +176,10 @@ inline int device_sm_count() {
 // Launchers (defined in the .cu files). Each returns the launch's CUDA error.
 cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps /*q,k,v,o*/,
                        const FwdParams& p, cudaStream_t stream);
+// The forward for head dims 136..256: one 128-row query tile per CTA
+// (p.n_q_tiles = ceil(Sq / 128)); maps q (box 64 x 128 rows), k, v (64 x 64).
+cudaError_t launch_fwd_d256(bool causal, bool dropout, const CUtensorMap* maps /*q,k,v*/,
+                            const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_preprocess(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_sum(const SumParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout,

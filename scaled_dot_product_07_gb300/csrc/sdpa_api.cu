@@ -242,14 +242,13 @@ size_t checked_bytes(int64_t a, int64_t b, int64_t c, int64_t d) {
   return static_cast<size_t>(a * b * c * d * 4);
 }
 
-// Head dims served: multiples of 8 up to 128. The kernels are built for 64
-// and 128; a smaller D runs the next larger one, with the missing columns of
-// q, k, v, dout read as zeros by the TMA loads (out-of-bounds fill) and never
-// written by the TMA stores (out-of-bounds elements are clipped). Zero
-// columns add nothing to Q K^T, dO V^T or any product, so the results are
-// those of the unpadded problem.
-bool head_dim_supported(int64_t D) { return D >= 8 && D <= 128 && D % 8 == 0; }
-int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : 128; }
+// Head dims served: multiples of 8 up to 256. The forward kernels are built
+// for 64, 128 and 256; a smaller D runs the next larger one, with the missing
+// columns of q, k, v, dout read as zeros by the TMA loads (out-of-bounds
+// fill) and never written by the stores. Zero columns add nothing to Q K^T,
+// dO V^T or any product, so the results are those of the unpadded problem.
+bool head_dim_supported(int64_t D) { return D >= 8 && D <= 256 && D % 8 == 0; }
+int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
 // The backward runs every head dim on the 128-wide kernel: at D=64 it beat a
 // 64-wide kernel of 128-row query steps (B8 H16 S4096 causal: 1.31 against
 // 1.41 ms; with dropout 0.1: 2.05 against 4.53 ms). The fp32 dQ rows of the
@@ -390,16 +389,19 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
                        uint64_t offset, const Opts& opt, const int32_t* cu_q, const int32_t* cu_k,
                        int64_t total_q, cudaStream_t stream) {
   const int64_t Dk = kernel_head_dim(D);
+  // the 256-wide forward streams 64-key K / V tiles
+  const uint32_t kv_rows = Dk == 256 ? 64 : 128;
   CUtensorMap maps[4];
-  if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, 128) || !make_map(&maps[2], v, 128) ||
-      !make_map(&maps[3], out, 128))
+  if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, kv_rows) ||
+      !make_map(&maps[2], v, kv_rows) || !make_map(&maps[3], out, 128))
     return SDPA_ERR_CUDA;
   FwdParams p;
   p.B = static_cast<int>(B);
   p.H = static_cast<int>(H);
   p.Sq = static_cast<int>(Sq);
   p.Sk = static_cast<int>(Sk);
-  p.n_q_tiles = static_cast<int>((Sq + 255) / 256);  // pairs of 128-row query tiles
+  // pairs of 128-row query tiles (one 128-row tile per CTA at D = 256)
+  p.n_q_tiles = static_cast<int>(Dk == 256 ? (Sq + 127) / 128 : (Sq + 255) / 256);
   p.scale_log2 = scale * kLog2e;
   p.drop_threshold = drop_threshold(dropout_p);
   p.drop_rescale = static_cast<float>(1.0 / (1.0 - dropout_p));
@@ -425,7 +427,9 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
   if (!p.err) return SDPA_ERR_CUDA;
   const bool dropout = dropout_p > 0.0;
   cudaError_t e = record_event(opt.ev_begin, stream);
-  if (e == cudaSuccess) e = launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream);
+  if (e == cudaSuccess)
+    e = Dk == 256 ? launch_fwd_d256(is_causal != 0, dropout, maps, p, stream)
+                  : launch_fwd(static_cast<int>(Dk), is_causal != 0, dropout, maps, p, stream);
   if (e == cudaSuccess) e = record_event(opt.ev_end, stream);
   return finish(e, stream);
 }
@@ -592,6 +596,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(out, B, H, Sq, D)) != SDPA_OK) return s;
+  if (D > 128 && options && options->attn_bias) return SDPA_ERR_UNSUPPORTED;
   if (B * H * Sq == 0) return SDPA_OK;
   if (Sk == 0) return SDPA_ERR_INVALID_ARG;  // softmax over no keys
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
@@ -657,7 +662,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if (s != SDPA_OK) return s;
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
-  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D) || D > 128) return SDPA_ERR_UNSUPPORTED;
   if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
@@ -711,7 +716,7 @@ sdpa_status sdpa_bwd_varlen(const sdpa_tensor* dout, const sdpa_tensor* q, const
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t H = q->size[1], Tq = q->size[2], Tk = k->size[2], D = q->size[3];
   if ((s = check_varlen(seqs, q, k)) != SDPA_OK) return s;
-  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D) || D > 128) return SDPA_ERR_UNSUPPORTED;
   if ((s = check_tensor(q, 1, H, Tq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, 1, H, Tk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, 1, H, Tk, D)) != SDPA_OK) return s;
