@@ -18,7 +18,7 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsdpa_gb300.so")
 OBJ_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["sdpa_api.cu", "sdpa_fwd.cu", "sdpa_fwd256.cu", "sdpa_bwd.cu", "sdpa_bwd128.cu",
-           "sdpa_noalloc.cu"]
+           "sdpa_bwd256.cu", "sdpa_noalloc.cu"]
 HEADERS = ["ptx.cuh", "philox.cuh", "common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -105,7 +105,7 @@ struct BwdParams {
 };
 
 
-// D is the backward kernel's head dim (128: the width of the fp32 dQ rows);
+// D is the backward kernel's head dim (128 or 256: the width of the fp32 dQ rows);
 // D_io the caller's head dim (a multiple of 8, at most D), the width of the
 // rows read from out / dout and written to dq.
 struct PreParams {
@@ -140,6 +140,15 @@ struct SumParams {
   size_t part_stride;
   StridedBf16 dq;
 };
+
+// Float offset of element (row i, column c) of (batch, head) bh in the fp32
+// dQ accumulator (or one deterministic-mode slice) of a backward of kernel
+// head dim D: the columns are split into blocks of 128, and each block's
+// rows are contiguous, [B*H][D/128][Sq_pad][128] (at D = 128 plain rows).
+__host__ __device__ __forceinline__ size_t dq_acc_offset(int64_t bh, int64_t i, int c, int D,
+                                                        int Sq_pad) {
+  return ((static_cast<size_t>(bh) * (D >> 7) + (c >> 7)) * Sq_pad + i) * 128 + (c & 127);
+}
 
 // Opt the kernel into `bytes` of dynamic shared memory, once per device: later
 // launches (including those recorded while a stream is being captured into a
@@ -187,6 +196,11 @@ cudaError_t launch_bwd_main(int D, bool causal, bool dropout,
                             cudaStream_t stream);
 cudaError_t launch_bwd_main_d128(bool causal, bool dropout,
                                  const CUtensorMap* maps /*q,k,v,do,dk,dv,bias,dbias,dq*/, const BwdParams& p,
+                                 cudaStream_t stream);
+// The backward for kernel head dim 256: two CTAs (column halves) per 128-key
+// tile; maps q, dout (box 64 x 32 rows), k, v, dk, dv (64 x 128).
+cudaError_t launch_bwd_main_d256(bool causal, bool dropout,
+                                 const CUtensorMap* maps /*q,k,v,do,dk,dv*/, const BwdParams& p,
                                  cudaStream_t stream);
 cudaError_t launch_bwd_dq_convert(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStream_t stream);

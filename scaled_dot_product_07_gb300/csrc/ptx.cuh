@@ -423,6 +423,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
   return d;
 }
 
+// The same descriptor for a 64-byte-swizzled tile of 64-byte rows (swizzle
+// mode 4; the pattern repeats every 512 bytes, 8 rows). K-major: SBO = 512
+// for packed 8-row groups; MN-major with an M/N extent of 32 elements: SBO =
+// distance between groups of 8 K-rows.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t smem_addr, uint32_t lbo_bytes,
+                                               uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16: bf16 x bf16 -> fp32, dense.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16)
 //   bit 15 A is MN-major; bit 16 B is MN-major; bits 17-22 N>>3; bits 24-28 M>>4
@@ -438,6 +453,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // CU_TENSOR_MAP_SWIZZLE_128B and tcgen05 reads with swizzle mode 2).
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..3) of row `row` inside a
+// 64-byte-swizzled tile of 64-byte rows (swizzle mode 4 of tcgen05: address
+// bits 4-5 XOR bits 7-8).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
+  return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
 }  // namespace sdpa

@@ -249,11 +249,12 @@ size_t checked_bytes(int64_t a, int64_t b, int64_t c, int64_t d) {
 // dO V^T or any product, so the results are those of the unpadded problem.
 bool head_dim_supported(int64_t D) { return D >= 8 && D <= 256 && D % 8 == 0; }
 int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256); }
-// The backward runs every head dim on the 128-wide kernel: at D=64 it beat a
-// 64-wide kernel of 128-row query steps (B8 H16 S4096 causal: 1.31 against
-// 1.41 ms; with dropout 0.1: 2.05 against 4.53 ms). The fp32 dQ rows of the
-// workspace are therefore 128 wide for every D.
-constexpr int64_t kBwdHeadDim = 128;
+// The backward runs every head dim up to 128 on the 128-wide kernel: at D=64
+// it beat a 64-wide kernel of 128-row query steps (B8 H16 S4096 causal: 1.31
+// against 1.41 ms; with dropout 0.1: 2.05 against 4.53 ms). Larger head dims
+// run the 256-wide kernel. The fp32 dQ rows of the workspace are as wide as
+// the kernel's head dim.
+int64_t bwd_kernel_head_dim(int64_t D) { return D <= 128 ? 128 : 256; }
 
 // Resolved sdpa_options.
 struct Opts {
@@ -445,7 +446,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
                        sdpa_tensor* dk, sdpa_tensor* dv, void* workspace, size_t workspace_bytes,
                        const sdpa_options* options, const Opts& opt, const int32_t* cu_q,
                        const int32_t* cu_k, int64_t total_q, cudaStream_t stream) {
-  const int64_t Dk = kBwdHeadDim;
+  const int64_t Dk = bwd_kernel_head_dim(D);
   const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SDPA_ERR_WORKSPACE;
@@ -468,7 +469,9 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   maps[6] = maps[0];
   maps[7] = maps[0];
   maps[8] = maps[0];
-  if (dq_acc != nullptr && !make_dq_map(&maps[8], dq_acc, B * H * Sq_pad)) return SDPA_ERR_CUDA;
+  // the packed-batch form of the 128-wide kernel reduces dQ through a 2-D map
+  if (Dk == 128 && dq_acc != nullptr && !make_dq_map(&maps[8], dq_acc, B * H * Sq_pad))
+    return SDPA_ERR_CUDA;
   if (opt.bias.data != nullptr &&
       !make_bias_map(&maps[6], opt.bias, opt.bias_B, opt.bias_H, Sq, Sk))
     return SDPA_ERR_CUDA;
@@ -641,14 +644,14 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D) {
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
-  return checked_bytes(B, H, round_up(Sq, 128), kBwdHeadDim + 2);
+  return checked_bytes(B, H, round_up(Sq, 128), bwd_kernel_head_dim(D) + 2);
 }
 
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
                                   const sdpa_options* options) {
   if (!options || !options->deterministic) return sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
-  return checked_bytes(B, H, round_up(Sq, 128), kBwdHeadDim * ((Sk + 127) / 128) + 2);
+  return checked_bytes(B, H, round_up(Sq, 128), bwd_kernel_head_dim(D) * ((Sk + 127) / 128) + 2);
 }
 
 sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,
@@ -662,7 +665,8 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if (s != SDPA_OK) return s;
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t B = q->size[0], H = q->size[1], Sq = q->size[2], Sk = k->size[2], D = q->size[3];
-  if (!head_dim_supported(D) || D > 128) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
+  if (D > 128 && options && (options->attn_bias || options->dbias)) return SDPA_ERR_UNSUPPORTED;
   if ((s = check_tensor(q, B, H, Sq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, B, H, Sk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, B, H, Sk, D)) != SDPA_OK) return s;
@@ -716,7 +720,7 @@ sdpa_status sdpa_bwd_varlen(const sdpa_tensor* dout, const sdpa_tensor* q, const
   if ((s = check_common(dropout_p, scale)) != SDPA_OK) return s;
   const int64_t H = q->size[1], Tq = q->size[2], Tk = k->size[2], D = q->size[3];
   if ((s = check_varlen(seqs, q, k)) != SDPA_OK) return s;
-  if (!head_dim_supported(D) || D > 128) return SDPA_ERR_UNSUPPORTED;
+  if (!head_dim_supported(D)) return SDPA_ERR_UNSUPPORTED;
   if ((s = check_tensor(q, 1, H, Tq, D)) != SDPA_OK) return s;
   if ((s = check_tensor(k, 1, H, Tk, D)) != SDPA_OK) return s;
   if ((s = check_tensor(v, 1, H, Tk, D)) != SDPA_OK) return s;
@@ -795,7 +799,7 @@ const char* sdpa_status_string(sdpa_status status) {
   switch (status) {
     case SDPA_OK: return "SDPA_OK";
     case SDPA_ERR_INVALID_ARG: return "SDPA_ERR_INVALID_ARG: invalid argument";
-    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported shape or layout (D a multiple of 8 in [8, 128], innermost)";
+    case SDPA_ERR_UNSUPPORTED: return "SDPA_ERR_UNSUPPORTED: unsupported shape, layout or option (D a multiple of 8 in [8, 256], innermost; no attention bias above D = 128 or with a packed batch)";
     case SDPA_ERR_ALIGNMENT: return "SDPA_ERR_ALIGNMENT: base pointers and strides must be 16-byte aligned";
     case SDPA_ERR_CUDA: return "SDPA_ERR_CUDA: CUDA launch or driver call failed";
     case SDPA_ERR_DEVICE_TIMEOUT: return "SDPA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";

@@ -9,7 +9,8 @@
 // Three kernels on one stream:
 //   bwd_preprocess_kernel  Delta_i = sum_e dO_ie * O_ie, lse * log2(e) into a
 //                          padded workspace (+inf past Sq), dQ accumulator := 0
-//   main kernel            (sdpa_bwd128.cu, every head dim on 128-wide tiles)
+//   main kernel            (sdpa_bwd128.cu for head dims up to 128 on 128-wide
+//                          tiles, sdpa_bwd256.cu above)
 //                          one CTA per 128-key tile of one (batch, head); it
 //                          walks the query steps that can see its keys and
 //                          reduce-adds each step's fp32 dQ partial
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const ConvParams p)
       tb = 0;
     }
     const float4* src =
-        reinterpret_cast<const float4*>(p.dq_acc + (bh * p.Sq_pad + i) * p.D + part * 8);
+        reinterpret_cast<const float4*>(p.dq_acc + dq_acc_offset(bh, i, part * 8, p.D, p.Sq_pad));
     const float4 a = src[0], c = src[1];
     uint4 o;
     o.x = pack_bf16x2(a.x * p.scale, a.y * p.scale);
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(256) bwd_dq_sum_kernel(const SumParams p) {
       tb = 0;
     }
     const int k_last = p.causal ? min(n_kv - 1, i / 128) : n_kv - 1;
-    const float* src = p.dq_part + (bh * p.Sq_pad + i) * p.D + part * 8;
+    const float* src = p.dq_part + dq_acc_offset(bh, i, part * 8, p.D, p.Sq_pad);
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int k = 0; k <= k_last; ++k) {
       const float4* s4 = reinterpret_cast<const float4*>(src + static_cast<size_t>(k) * p.part_stride);
@@ -226,8 +227,10 @@ cudaError_t launch_zero_fill(StridedBf16 t, int B, int H, int S, int D, cudaStre
 
 cudaError_t launch_bwd_main(int D, bool causal, bool dropout, const CUtensorMap* maps,
                             const BwdParams& p, cudaStream_t stream) {
-  // every head dim runs the 128-wide kernel (sdpa_bwd128.cu)
+  // head dims up to 128 run the 128-wide kernel (sdpa_bwd128.cu), larger ones
+  // the 256-wide kernel (sdpa_bwd256.cu)
   if (D == 128) return launch_bwd_main_d128(causal, dropout, maps, p, stream);
+  if (D == 256) return launch_bwd_main_d256(causal, dropout, maps, p, stream);
   return cudaErrorInvalidValue;
 }
 

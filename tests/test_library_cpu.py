@@ -58,9 +58,12 @@ def test_workspace_size(lib):
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(8, 16, 4096, 4096, 128) == 8 * 16 * 4096 * 130 * 4
     assert sdpa.sdpa_bwd_workspace_size(0, 3, 200, 77, 64) == 0
-    # the backward runs every head dim on 128-wide tiles: 128-wide accumulator rows
+    # the backward runs every head dim up to 128 on 128-wide tiles: 128-wide
+    # accumulator rows; above 128 on 256-wide tiles
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 96) == 2 * 3 * 256 * (128 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 136) == 2 * 3 * 256 * (256 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 256) == 2 * 3 * 256 * (256 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(1, 1, 0, 77, 64) == 0
 
 
@@ -98,8 +101,8 @@ def fwd_status(lib, q, k, v, o, p=0.0, causal=0, scale=0.125, lse=FAKE):
 def test_forward_argument_errors(lib):
     B, H, S, D = 2, 3, 100, 64
     ok = lambda: desc(B, H, S, D)
-    # head dims: multiples of 8 up to 128
-    for bad in (100, 136, 4):
+    # head dims: multiples of 8 up to 256
+    for bad in (100, 264, 4, 130):
         assert fwd_status(lib, desc(B, H, S, bad), desc(B, H, S, bad), desc(B, H, S, bad),
                           desc(B, H, S, bad)) == 2
     # E != Ev

@@ -33,7 +33,7 @@ def _inputs(B, H, Sq, Sk, D, input_seed):
     return W.draw_inputs(w)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_graph_replay_with_device_rng_matches_host_seeded_calls(cuda_lib, D):
     sdpa = cuda_lib
     B, H, Sq, Sk, p = 1, 2, 300, 300, 0.2
@@ -93,7 +93,7 @@ def test_shard_mask_is_the_slice_of_the_whole_mask(cuda_lib, B, H, Sq, Sk, b0, h
     assert torch.equal(part, part2)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_sharded_call_matches_the_oracle_on_global_heads(cuda_lib, D, causal):
     B, H, Sq, Sk, p = 2, 4, 200, 330, 0.25
@@ -118,7 +118,7 @@ def test_sharded_call_matches_the_oracle_on_global_heads(cuda_lib, D, causal):
     compare(full, ref, heads, f"shard D{D} causal{int(causal)}")
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("p", [0.0, 0.2])
 @pytest.mark.parametrize("Sq,Sk", [(300, 460), (460, 200)])

@@ -267,25 +267,20 @@ def test_other_head_dims_parity(cuda_lib, D, causal, p):
     compare(gpu, ref, heads, f"D{D} c{int(causal)} p{p} {layout}")
 
 
-# head dims above 128 (multiples of 8 up to 256): the 256-wide forward with
-# the missing columns zero-filled by TMA; ragged query and key tails, key
-# counts that are and are not multiples of 4 (the two dropout draw paths)
+# head dims above 128 (multiples of 8 up to 256): the 256-wide forward and
+# backward with the missing columns zero-filled by TMA; ragged query and key
+# tails, key counts that are and are not multiples of 4 (the two dropout
+# draw paths)
 @pytest.mark.parametrize("D", [136, 192, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("p", [0.0, 0.15])
 @pytest.mark.parametrize("Sq,Sk", [(200, 332), (333, 301)])
-def test_wide_head_dims_forward_parity(cuda_lib, D, causal, p, Sq, Sk):
+def test_wide_head_dims_parity(cuda_lib, D, causal, p, Sq, Sk):
     w = W.Workload("wide", 1, 2, Sq, Sk, D, causal, p, seed=11 + D, offset=D + Sk,
                    input_seed=900 + D + Sq)
     inputs = W.draw_inputs(w)
     layout = "BSHE" if D == 192 else "BHSE"
-    q, k, v, _ = (W.to_layout(x, layout).cuda() for x in inputs)
-    out, lse, _, _ = cuda_lib.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset)
-    torch.cuda.synchronize()
-    assert cuda_lib.sdpa_check_device() == 0
-    f64 = [x.float().numpy().astype(np.float64) for x in inputs]
-    ro, rl = oracle.sdpa_fwd(f64[0], f64[1], f64[2], w.dropout_p, w.is_causal, None, w.seed,
-                             w.offset)
-    err_o = np.abs(to_np(out) - ro).max()
-    err_l = np.abs(to_np(lse) - rl).max()
-    assert err_o <= OUT_ATOL and err_l <= LSE_ATOL, (err_o, err_l)
+    gpu = run_gpu(cuda_lib, w, inputs, layout)
+    heads = [(0, h) for h in range(w.H)]
+    ref = oracle_heads(w, inputs, heads)
+    compare(gpu, ref, heads, f"D{D} c{int(causal)} p{p} {Sq}x{Sk} {layout}")

@@ -81,7 +81,7 @@ def check_against_oracle(inputs, gpu, lens_q, lens_k, Mq, Mk, H, p, causal, tag,
             assert e <= GRAD_RTOL_L2, f"{msg}: {n} rel L2 {e:.3g}"
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("p", [0.0, 0.2])
 def test_varlen_parity(cuda_lib, D, causal, p):
@@ -108,9 +108,10 @@ def test_varlen_equals_the_fixed_length_call_when_all_lengths_match(cuda_lib):
     assert torch.equal(gpu[1].reshape(H, B, S).permute(1, 0, 2), lse)
 
 
-def test_varlen_deterministic_backward_is_reproducible(cuda_lib):
+@pytest.mark.parametrize("D", [128, 200])
+def test_varlen_deterministic_backward_is_reproducible(cuda_lib, D):
     lens_q, lens_k = [100, 260], [300, 90]
-    runs = [run_varlen(cuda_lib, lens_q, lens_k, 260, 300, 2, 128, 0.1, True, deterministic=True)
+    runs = [run_varlen(cuda_lib, lens_q, lens_k, 260, 300, 2, D, 0.1, True, deterministic=True)
             for _ in range(2)]
     for a, b in zip(runs[0][1][2:], runs[1][1][2:]):
         assert torch.equal(a, b)
