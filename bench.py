@@ -684,8 +684,8 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
                                        "the mask is regenerated in the backward", peak)
 
     # other head dims on the same B, H, S: 96 (the 128-wide kernels with the
-    # last 32 columns zero-filled by TMA)
-    for D in (96,):
+    # last 32 columns zero-filled by TMA) and 256 (the 256-wide kernels)
+    for D in (96, 256):
         wd = W.Workload(f"{w.name}_d{D}", w.B, w.H, w.Sq, w.Sk, D, w.is_causal, w.dropout_p,
                         seed=w.seed, offset=w.offset, input_seed=w.input_seed)
         gd = torch.Generator(device="cpu")

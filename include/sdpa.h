@@ -22,9 +22,11 @@
  *   two layouts of test_sdpa_loop_split. Strides of dims of size > 1 must be
  *   multiples of 8 elements (16 bytes) and every base pointer 16-byte aligned.
  * - D (= E = Ev, the head dim of q, k and v) must be a multiple of 8 from 8
- *   to 128. The kernels are built for 64 and 128; a smaller D runs the next
- *   larger one, the missing columns being read as zeros by the TMA loads and
- *   clipped from the TMA stores, so the results are those of D itself.
+ *   to 256. The kernels are built for 64, 128 and 256 (the backward for 128
+ *   and 256); a smaller D runs the next larger one, the missing columns being
+ *   read as zeros by the TMA loads and never stored, so the results are those
+ *   of D itself. An attention bias (sdpa_options.attn_bias) is served up to
+ *   D = 128.
  * - Causal masking is top-left aligned: key j is visible to query i iff j <= i.
  * - Ownership: the caller allocates every input, output and workspace; the
  *   library allocates no device memory and keeps no per-call state. Work is
@@ -62,7 +64,8 @@ typedef struct {
 typedef enum {
   SDPA_OK = 0,
   SDPA_ERR_INVALID_ARG = 1,    /* shape mismatch, null pointer, p outside [0,1), bad scale */
-  SDPA_ERR_UNSUPPORTED = 2,    /* D not a multiple of 8 in [8, 128], D not innermost, or
+  SDPA_ERR_UNSUPPORTED = 2,    /* D not a multiple of 8 in [8, 256], D not innermost, an
+                                  attention bias with D > 128 or a packed batch, or
                                   B*H*ceil(max(Sq, Sk)/128) above 2^31-1 (launch grids) */
   SDPA_ERR_ALIGNMENT = 3,      /* base or stride not 16-byte aligned */
   SDPA_ERR_CUDA = 4,           /* a CUDA launch or driver call failed */
@@ -92,9 +95,10 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 
 /*
  * sdpa_bwd_workspace_size — bytes of device workspace sdpa_bwd needs for
- * this problem size: an fp32 dQ accumulator of 128-wide rows (the backward
- * runs every head dim on 128-wide tiles) and two fp32 row vectors, with Sq
- * rounded up to a multiple of 128: B*H*ceil128(Sq)*(128 + 2)*4 bytes.
+ * this problem size: an fp32 dQ accumulator of Dk-wide rows (Dk = 128 for
+ * D <= 128, whose backward runs on 128-wide tiles, and 256 above) and two
+ * fp32 row vectors, with Sq rounded up to a multiple of 128:
+ * B*H*ceil128(Sq)*(Dk + 2)*4 bytes.
  * Returns 0 for an empty problem, and SIZE_MAX when the size does not fit in
  * 62 bits (no workspace then satisfies sdpa_bwd, which returns
  * SDPA_ERR_WORKSPACE).
@@ -238,7 +242,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
 /*
  * sdpa_bwd_workspace_size_ex — workspace bytes of sdpa_bwd_ex with these
  * options: sdpa_bwd_workspace_size(), or in deterministic mode one fp32 dQ
- * slice per 128-key tile, B*H*ceil128(Sq)*(128*ceil(Sk/128) + 2)*4 bytes
+ * slice per 128-key tile, B*H*ceil128(Sq)*(Dk*ceil(Sk/128) + 2)*4 bytes
  * (SIZE_MAX when that does not fit in 62 bits).
  */
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,

@@ -11,7 +11,7 @@ library is missing or no GPU is present the calls raise.
     dq, dk, dv = sdpa_bwd(dout, q, k, v, out, lse, dropout_p, is_causal,
                           seed, offset, scale)
 
-Tensors have the logical shape [B, H, S, D] (D a multiple of 8 up to 128,
+Tensors have the logical shape [B, H, S, D] (D a multiple of 8 up to 256,
 innermost and contiguous) in bfloat16, in any dense order of B, H, S with 16-byte aligned
 strides -- e.g. BHSE or BSHE ("DID loop split for SDPA", NVIDIA/Fuser PR
 3711, test_sdpa_loop_split). ``lse`` is float32 [B, H, Sq].

@@ -32,5 +32,5 @@ def test_default_bench_path_prints_a_complete_line(cuda_lib):
     assert line["cpu_baseline"]["cores"] >= 1
     assert line["sustained"]["steps"] > 0
     for name in ("graph_step", "bwd_deterministic", "dropout_0.1", "attn_bias", "varlen",
-                 "pages_test", "encoder_dropout", "cross_attn"):
+                 "head_dim_96", "head_dim_256", "pages_test", "encoder_dropout", "cross_attn"):
         assert name in line["extended"], name
