@@ -78,6 +78,23 @@ struct FwdLayout {
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
+// The forward with a bias keeps the same Q, K and V tiles and adds a 32 KB
+// staging area: each softmax thread's 64 bias values of its next tile (128
+// bytes), copied asynchronously while it works on the current one. To make
+// room, the row-max exchange between the two halves of a row uses one slot
+// per (half, row) instead of four.
+template <int D>
+struct FwdBiasLayout : FwdLayout<D> {
+  using Base = FwdLayout<D>;
+  static constexpr int kRed = Base::kRed;                 // [half 2][row 128] fp32
+  static constexpr int kBar = kRed + 2 * 128 * 4;
+  static constexpr int kMisc = kBar + Base::kNumBars * 8;
+  static constexpr int kBiasStage = (kMisc + 16 + 127) / 128 * 128;  // [thread 256][128 bytes]
+  static constexpr int kBytes = kBiasStage + 256 * 128;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "shared memory budget");
+};
+
 __device__ __forceinline__ void reg_touch(uint32_t (&r)[32]) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
@@ -557,7 +574,7 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   constexpr bool BIAS = true;
-  using L = FwdLayout<D>;
+  using L = FwdBiasLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -734,17 +751,58 @@ __global__ void __launch_bounds__(320, 1)
     const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
     float m[2] = {-INFINITY, -INFINITY};  // running max of the raw scores of the row, per tile
     float l[2] = {0.f, 0.f};              // this half's running sum, per tile
-    // the half's tile max, shared with the partner half; returns the row's tile max
-    auto exchange_max = [&](int i, int j, float mh) {
-      float* slot = red + ((i * 2 + (j & 1)) * 2) * 128;
-      slot[half * 128 + row] = mh;
+    // the half's value v, shared with the partner half through the pair's one
+    // slot: the first barrier makes sure the partner has read the previous
+    // value, the second that it has written this one
+    auto exchange = [&](int i, float v) {
+      named_barrier_sync(pair_bar + 4 * i, 64);
+      red[half * 128 + row] = v;
       // also orders the partner's TMEM score reads before this warp's P
       // stores into the same columns
       tc_fence_before();
       named_barrier_sync(pair_bar + 4 * i, 64);
       tc_fence_after();
-      return fmaxf(mh, slot[(1 - half) * 128 + row]);
+      return red[(1 - half) * 128 + row];
     };
+    // the half's tile max, shared with the partner half; returns the row's tile max
+    auto exchange_max = [&](int i, int j, float mh) {
+      (void)j;
+      return fmaxf(mh, exchange(i, mh));
+    };
+    // The bias values of tile (i, j) for this thread -- keys [j*128 + 64 half,
+    // +64) of row q0 + 128 i + row -- copied asynchronously into its own 128
+    // bytes of the staging area (16-byte chunks placed so that a warp's
+    // reads of one chunk hit distinct banks). Keys past Sk read as zeros.
+    const uint32_t bstage = sb + L::kBiasStage + (half * 128 + row) * 128;
+    auto fetch_bias = [&](int i, int j) {
+      const int kb = j * 128 + 64 * half;
+      const uint16_t* rp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
+                           static_cast<int64_t>(min(q0 + 128 * i + row, Sq - 1)) * p.bias.sS;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int nv = min(max(Sk - (kb + 8 * c), 0), 8);
+        cp_async16(bstage + ((c ^ (row & 7)) << 4), nv > 0 ? rp + kb + 8 * c : rp, 2 * nv);
+      }
+      cp_async_commit();
+    };
+    // the tile after (i, j) in the order the loop visits them
+    auto next_tile = [&](int i, int j, int& i2, int& j2) {
+      for (;;) {
+        if (i == 0) {
+          i = 1;
+        } else {
+          i = 0;
+          ++j;
+        }
+        if (j >= n_kv) return false;
+        if (j < n_t[i]) {
+          i2 = i;
+          j2 = j;
+          return true;
+        }
+      }
+    };
+    if (n_kv > 0) fetch_bias(n_t[0] > 0 ? 0 : 1, 0);
 
     for (int j = 0; j < n_kv; ++j) {
       for (int i = 0; i < 2; ++i) {
@@ -752,35 +810,12 @@ __global__ void __launch_bounds__(320, 1)
         const int qi = q0 + 128 * i + row;
         const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
         const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-        // the half row's 64 bias values, fetched before the scores are ready
+        // the half row's 64 bias values: this tile's copy (issued one tile
+        // ahead) has landed
         uint4 bv[8];
-        if (BIAS) {
-          // start the next key tile's bias line towards L2
-          const int kn = (j + 1) * 128 + 64 * half;
-          if (j + 1 < n_t[i] && kn < Sk) {
-            const uint16_t* np = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                                 static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kn;
-            prefetch_l2(np);
-            prefetch_l2(np + min(56, Sk - 1 - kn));
-          }
-          const int kb = j * 128 + 64 * half;
-          const uint16_t* bp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                               static_cast<int64_t>(min(qi, Sq - 1)) * p.bias.sS + kb;
+        cp_async_wait_all();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            if (kb + 8 * c + 8 <= Sk) {
-              bv[c] = __ldg(reinterpret_cast<const uint4*>(bp + 8 * c));
-            } else {
-              // key tail: only the keys that exist are read
-              uint32_t w[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-              for (int e = 0; e < 8; ++e)
-                if (kb + 8 * c + e < Sk)
-                  w[e >> 1] |= static_cast<uint32_t>(__ldg(bp + 8 * c + e)) << (16 * (e & 1));
-              bv[c] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-        }
+        for (int c = 0; c < 8; ++c) bv[c] = ld_shared_v4(bstage + ((c ^ (row & 7)) << 4));
         mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
         tc_fence_after();
         uint32_t r0[32], r1[32];
@@ -806,6 +841,9 @@ __global__ void __launch_bounds__(320, 1)
               x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
             }
           }
+          // the staging slot is free again: start the next tile's copy
+          int i2 = 0, j2 = 0;
+          if (next_tile(i, j, i2, j2)) fetch_bias(i2, j2);
         }
         const int k0 = j * 128 + 64 * half;  // first key of this half
         if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
@@ -884,14 +922,8 @@ __global__ void __launch_bounds__(320, 1)
       if (n_t[i] == 0) continue;
       const int qi = q0 + 128 * i + row;
       const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-      // the row sum is the sum of both halves (slot parity n_t[i] is unused by
-      // the last tile's max exchange)
-      const float l_row = [&] {
-        float* slot = red + ((i * 2 + (n_t[i] & 1)) * 2) * 128;
-        slot[half * 128 + row] = l[i];
-        named_barrier_sync(pair_bar + 4 * i, 64);
-        return l[i] + slot[(1 - half) * 128 + row];
-      }();
+      // the row sum is the sum of both halves
+      const float l_row = l[i] + exchange(i, l[i]);
       mbar_wait(&o_full[i], 0, wc, kSiteFwdODone);
       tc_fence_after();
       // 1/l, and the dropout rescale 1/(1-p) of the kept weights
@@ -962,7 +994,7 @@ cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream
 template <int D, bool C, bool DR>
 cudaError_t launch_fwd_bias_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
   auto kern = fwd_kernel_bias<D, C, DR>;
-  const int smem = FwdLayout<D>::kAlloc;
+  const int smem = FwdBiasLayout<D>::kAlloc;
   cudaError_t e = ensure_smem_attr<fwd_kernel_bias<D, C, DR>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
