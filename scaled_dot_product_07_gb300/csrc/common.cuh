@@ -95,6 +95,7 @@ struct BwdParams {
   int Sq_ctr, Sk_ctr;       // dims of the dropout counter
   int D_io;                 // the caller's head dim (columns of dk, dv)
   StridedBf16 dk_io, dv_io; // for the direct stores of a sequence's last key tile
+  StridedBf16 k_io;         // k, read row by row by the 256-wide kernel (K into TMEM)
   float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
   float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
   size_t part_stride;     // one plain-stored partial per key tile (floats per slice)

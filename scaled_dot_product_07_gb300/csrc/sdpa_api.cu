@@ -527,6 +527,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   p.D_io = static_cast<int>(D);
   p.dk_io = strided(dk);
   p.dv_io = strided(dv);
+  p.k_io = strided(k);
   p.dq_acc = dq_acc;
   p.dq_part = opt.det ? dq_region : nullptr;
   p.part_stride = static_cast<size_t>(slice);

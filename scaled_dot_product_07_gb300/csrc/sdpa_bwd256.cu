@@ -9,9 +9,11 @@
 // one per 128-column half of D: CTA half hd keeps dK[:, hd] and dV[:, hd]
 // (128 columns each) and produces dQ[:, hd]. Both CTAs of a tile contract
 // the full D for S^T = K Q^T and dP~^T = V dO^T (7/5 of the algorithmic
-// flops). K and V (64 KB each) stay resident, so the query steps are 32 rows
-// (Q and dO 16 KB each per stage, 2 stages). 448 threads:
-//   warp 13     TMA: K, V once; Q_t, dO_t, lse2_t, Delta_t through the ring
+// flops). K is the A operand of S^T = K Q^T straight from TMEM (128 columns
+// of bf16 pairs, stored there once by compute warpgroup A), so shared memory
+// keeps only K[:, hd] (32 KB, for dQ) and V (64 KB), and the query steps are
+// 32 rows (Q and dO 16 KB each per stage, 3 stages). 448 threads:
+//   warp 13     TMA: K[:, hd], V once; Q_t, dO_t, lse2_t, Delta_t through the ring
 //   warp 12     TMEM allocator and MMA issuer (converged warp, elected lane)
 //   warps 0-3   compute warpgroup A (even steps), warps 4-7 B (odd steps):
 //               thread = key row. P~^T (bf16) goes to TMEM as the A operand
@@ -22,8 +24,8 @@
 //               fp32 and reduces it into this half's rows of the fp32
 //               accumulator (layout [B*H][2][Sq_pad][128]) with four bulk
 //               reduce-adds.
-// TMEM: dV [0,128), dK [128,256), and two step buffers {S^T (32 columns),
-// dP^T (32)} at 256 + 64 b; a step's dQ^T partial (128 lanes = d, 32
+// TMEM: dV [0,128), dK [128,256), two step buffers {S^T (32 columns),
+// dP^T (32)} at 256 + 64 b, and K [384,512); a step's dQ^T partial (128 lanes = d, 32
 // columns) overwrites its dP^T columns once the compute warpgroup has read
 // them. MMA order per step t: S^T(t), dP^T(t), then dV, dK, dQ of step t-1.
 #include "common.cuh"
@@ -33,15 +35,15 @@ namespace {
 
 struct B256 {
   static constexpr int kMq = 32;                  // query rows per step
-  static constexpr int kStages = 2;               // Q / dO ring
+  static constexpr int kStages = 3;               // Q / dO ring
   static constexpr int kKvSlab = 128 * 128;       // 128 keys x 64 columns bf16 (16 KB)
   static constexpr int kKvBytes = 4 * kKvSlab;    // 64 KB
   static constexpr int kQSlab = kMq * 128;        // 32 rows x 64 columns (4 KB)
   static constexpr int kQBytes = 4 * kQSlab;      // 16 KB
   static constexpr int kDsBytes = 128 * kMq * 2;  // [128 keys x 32 rows] bf16, 64-byte rows (8 KB)
   static constexpr int kDqBytes = kMq * 128 * 4;  // [32 rows x 128 d] fp32 staging (16 KB)
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kKvBytes;
+  static constexpr int kK = 0;                    // K[:, hd]: two slabs
+  static constexpr int kV = kK + 2 * kKvSlab;
   static constexpr int kQ = kV + kKvBytes;
   static constexpr int kDO = kQ + kStages * kQBytes;
   static constexpr int kDs = kDO + kStages * kQBytes;  // [2]
@@ -50,14 +52,16 @@ struct B256 {
   static constexpr int kDelta = kLse + kStages * kMq * 4;  // [kStages][32] fp32
   static constexpr int kBar = kDelta + kStages * kMq * 4;
   // kv_full, q_full[S], q_empty[S], and per step buffer b in {0,1}:
-  // s_full, dp_full, p_full, ds_full, sp_empty, dq_full, dq_empty, ds_empty; done
-  static constexpr int kNumBars = 1 + 2 * kStages + 8 * 2 + 1;
+  // s_full, dp_full, p_full, ds_full, sp_empty, dq_full, dq_empty, ds_empty;
+  // done, ktm_full (K stored in TMEM)
+  static constexpr int kNumBars = 1 + 2 * kStages + 8 * 2 + 2;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t kTmemDV = 0, kTmemDK = 128, kTmemCols = 512;
   __host__ __device__ static constexpr uint32_t tmem_s(int b) { return 256u + 64u * b; }
   __host__ __device__ static constexpr uint32_t tmem_dp(int b) { return 288u + 64u * b; }
+  static constexpr uint32_t kTmemK = 384;  // K as bf16 pairs, 128 columns
   static constexpr int kThreads = 448;
   static_assert(kAlloc <= 232448, "shared memory budget");
   static_assert(kDs % 1024 == 0, "dS^T tiles on swizzle-pattern boundaries");
@@ -93,6 +97,7 @@ __global__ void __launch_bounds__(448, 1)
   uint64_t* dq_empty = dq_full + 2;
   uint64_t* ds_empty = dq_empty + 2;
   uint64_t* done = ds_empty + 2;
+  uint64_t* ktm_full = done + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
 
@@ -145,6 +150,7 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&ds_empty[x], 1);
     }
     mbar_init(done, 1);
+    mbar_init(ktm_full, 128);
     *abort_word = 0u;
     fence_mbar_init();
   }
@@ -163,12 +169,14 @@ __global__ void __launch_bounds__(448, 1)
     if (lane == 0 && n_steps > 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kKvBytes);
+      mbar_arrive_expect_tx(kv_full, 6 * L::kKvSlab);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, s * 64, ks + k0, h, tb);
+      for (int s = 0; s < 4; ++s)
         tma_load_4d(smem + L::kV + s * L::kKvSlab, &tm_v, kv_full, s * 64, ks + k0, h, tb);
-      }
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        tma_load_4d(smem + L::kK + s * L::kKvSlab, &tm_k, kv_full, (2 * hd + s) * 64, ks + k0, h,
+                    tb);
       int t = 0;
       for (; t < n_steps; ++t) {
         const int st = t % NS;
@@ -204,11 +212,10 @@ __global__ void __launch_bounds__(448, 1)
       constexpr uint32_t kIdSP = idesc_bf16_f32(128, MQ, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKV = idesc_bf16_f32(128, 128, false, true);  // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, MQ, true, true);     // dQ^T
-      const uint64_t kd_k = sdesc_sw128(sb + L::kK, 16, 1024);  // K, K-major (M = keys, K = d)
       const uint64_t kd_v = sdesc_sw128(sb + L::kV, 16, 1024);  // V, K-major
       // K[:, hd] as the MN-major A operand of dQ^T (M = 128 d in two 64-column
       // slabs, K = keys)
-      const uint64_t kd_kmn = sdesc_sw128(sb + L::kK + hd * 2 * L::kKvSlab, L::kKvSlab, 1024);
+      const uint64_t kd_kmn = sdesc_sw128(sb + L::kK, L::kKvSlab, 1024);
       auto finish_step = [&](int u) {
         const int x = u & 1;
         const int st = u % NS;
@@ -245,6 +252,8 @@ __global__ void __launch_bounds__(448, 1)
         mma_commit_if(leader, &ds_empty[x]);
       };
       mbar_wait_t<kInlineWaits>(kv_full, 0, wc, kSiteBwdKvFull);
+      mbar_wait_t<kInlineWaits>(ktm_full, 0, wc, kSiteBwdKvFull);
+      tc_fence_after();
       for (int t = 0; t < n_steps; ++t) {
         const int x = t & 1;
         const int st = t % NS;
@@ -253,13 +262,13 @@ __global__ void __launch_bounds__(448, 1)
         mbar_wait_t<kInlineWaits>(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
         if (t >= 2) mbar_wait_t<kInlineWaits>(&sp_empty[x], ((t >> 1) - 1) & 1, wc, kSiteBwdSpEmpty);
         tc_fence_after();
-        // S^T = K Q^T (M = 128 keys, N = 32 rows, K = 256 d)
+        // S^T = K Q^T (M = 128 keys, N = 32 rows, K = 256 d): K from TMEM, 16
+        // d (8 columns) per product
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kKvSlab + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
-          mma_bf16_ss_if(leader, tmem + L::tmem_s(x), sdesc_add(kd_k, koff), sdesc_add(d_q, qoff),
-                         kIdSP, kk > 0 ? 1u : 0u);
+          mma_bf16_ts_if(leader, tmem + L::tmem_s(x), tmem + L::kTmemK + kk * 8,
+                         sdesc_add(d_q, qoff), kIdSP, kk > 0 ? 1u : 0u);
         }
         mma_commit_if(leader, &s_full[x]);
         // the dP^T columns held dQ^T(t-2) until the dQ warpgroup read it out
@@ -293,6 +302,31 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t tDP = tmem + L::tmem_dp(x) + lane_base;
     const uint32_t da = sb + L::kDs + x * L::kDsBytes;
     const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
+    if (x == 0 && n_steps > 0) {
+      // K row kj (all 256 columns) into TMEM lane r as bf16 pairs: column c
+      // holds elements 2c, 2c+1 (zeros past Sk and past the caller's D)
+      const uint16_t* krow = static_cast<const uint16_t*>(p.k_io.data) + tb * p.k_io.sB +
+                             h * p.k_io.sH + static_cast<int64_t>(ks + kj) * p.k_io.sS;
+      const uint32_t tK = tmem + L::kTmemK + lane_base;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {  // 64 elements, 32 columns, at a time
+        uint32_t w[32];
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {
+          const int e0 = cc * 64 + q8 * 8;
+          uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+          if (kj < Sk && e0 < p.D_io) v4 = *reinterpret_cast<const uint4*>(krow + e0);
+          w[4 * q8 + 0] = v4.x;
+          w[4 * q8 + 1] = v4.y;
+          w[4 * q8 + 2] = v4.z;
+          w[4 * q8 + 3] = v4.w;
+        }
+        tmem_st32(tK + cc * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ktm_full);
+    }
     for (int t = x, k = 0; t < n_steps; t += 2, ++k) {
       const int st = t % NS;
       const int i0 = (qt_first + t) * MQ;
