@@ -7,9 +7,10 @@
 //
 // At D = 256 a 128-row query tile is 64 KB of bf16 and its O accumulator
 // fills 256 of the 512 TMEM columns, so a CTA holds one query tile and
-// streams 64-key K and V tiles (32 KB each) through 2-stage rings:
-// Q 64 KB + K 64 KB + V 64 KB of shared memory. 320 threads:
-//   warp 9      TMA producer: Q once, then K_j and V_j (separate barriers).
+// streams 64-key K and V tiles (32 KB each) through one 5-slot ring in the
+// order K_0, V_0, K_1, V_1, ... (Q 64 KB + 160 KB of shared memory); a slot
+// is refilled once the product that reads it is done. 320 threads:
+//   warp 9      TMA producer: Q once, then K_j and V_j into the ring.
 //   warp 8      TMEM allocator and MMA issuer (converged warp, one elected
 //               lane issues). TMEM: S[2] (64 fp32 columns each, by key-tile
 //               parity) and O (256 columns). Per key tile j it issues
@@ -42,16 +43,15 @@ struct Fwd256Layout {
   static constexpr int kQSlab = 128 * 128;   // 128 rows x 64 columns bf16
   static constexpr int kKVSlab = 64 * 128;   // 64 keys x 64 columns bf16
   static constexpr int kQBytes = 4 * kQSlab;    // 64 KB
-  static constexpr int kKVBytes = 4 * kKVSlab;  // 32 KB per stage
-  static constexpr int kStages = 2;
+  static constexpr int kKVBytes = 4 * kKVSlab;  // 32 KB per slot
+  static constexpr int kSlots = 5;              // K / V ring
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + kStages * kKVBytes;
-  // row-max / row-sum exchange between the two halves of a row: [parity 2][half 2][row 128] fp32
-  static constexpr int kRed = kV + kStages * kKVBytes;
-  static constexpr int kBar = kRed + 2 * 2 * 128 * 4;
-  // q_full, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], pv_done
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
+  static constexpr int kKV = kQ + kQBytes;
+  // row-max / row-sum exchange between the two halves of a row: [half 2][row 128] fp32
+  static constexpr int kRed = kKV + kSlots * kKVBytes;
+  static constexpr int kBar = kRed + 2 * 128 * 4;
+  // q_full, full[slots], empty[slots], s_full[2], p_full[2], pv_done
+  static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 2 + 1;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align to 1024
@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(320, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
   using L = Fwd256Layout;
-  constexpr int S = L::kStages;
+  constexpr int NSL = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -120,11 +120,9 @@ __global__ void __launch_bounds__(320, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + S;
-  uint64_t* k_empty = v_full + S;
-  uint64_t* v_empty = k_empty + S;
-  uint64_t* s_full = v_empty + S;  // [2]
+  uint64_t* kv_full = bars + 1;       // [slots]
+  uint64_t* kv_empty = kv_full + NSL;  // [slots]
+  uint64_t* s_full = kv_empty + NSL;  // [2]
   uint64_t* p_full = s_full + 2;   // [2]
   uint64_t* pv_done = p_full + 2;  // one phase per P V product
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
@@ -136,11 +134,9 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int s = 0; s < NSL; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -160,6 +156,7 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl wc{abort_word, p.err, p.wait_limit_ns};
   const int n_kv = it.n_kv;
+  // ring item n: K_{n/2} (n even) or V_{n/2} (n odd), in slot n % slots
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
@@ -172,35 +169,26 @@ __global__ void __launch_bounds__(320, 1)
       for (int s = 0; s < 4; ++s)
         tma_load_4d(smem + L::kQ + s * L::kQSlab, &tm_q, q_full, s * 64, it.qs + it.q0, it.h,
                     it.tb);
-      int g = 0;
-      for (; g < n_kv; ++g) {
-        const int st = g % S;
-        // a K stage is free once the S product reading it is done, a V stage
-        // once the P V product reading it is done
-        if (g >= S) mbar_wait(&k_empty[st], ((g / S) - 1) & 1, wc, kSiteFwdKvEmpty);
-        mbar_arrive_expect_tx(&k_full[st], L::kKVBytes);
+      int n = 0;
+      for (; n < 2 * n_kv; ++n) {
+        const int sl = n % NSL;
+        // a slot is free once the product reading its previous item is done
+        if (n >= NSL) mbar_wait(&kv_empty[sl], ((n / NSL) - 1) & 1, wc, kSiteFwdKvEmpty);
+        mbar_arrive_expect_tx(&kv_full[sl], L::kKVBytes);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          tma_load_4d(smem + L::kK + st * L::kKVBytes + s * L::kKVSlab, &tm_k, &k_full[st],
-                      s * 64, it.ks + g * 64, it.h, it.tb);
-        if (g >= S) mbar_wait(&v_empty[st], ((g / S) - 1) & 1, wc, kSiteFwdKvEmpty);
-        mbar_arrive_expect_tx(&v_full[st], L::kKVBytes);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          tma_load_4d(smem + L::kV + st * L::kKVBytes + s * L::kKVSlab, &tm_v, &v_full[st],
-                      s * 64, it.ks + g * 64, it.h, it.tb);
+          tma_load_4d(smem + L::kKV + sl * L::kKVBytes + s * L::kKVSlab, (n & 1) ? &tm_v : &tm_k,
+                      &kv_full[sl], s * 64, it.ks + (n >> 1) * 64, it.h, it.tb);
         if (*abort_word) {
-          ++g;
+          ++n;
           break;
         }
       }
       if (*abort_word) {
         // give the loads still in flight time to land before the CTA exits
         mbar_wait_drain(q_full, 0, 2000000ull);
-        for (int gg = max(0, g - S); gg < g; ++gg) {
-          mbar_wait_drain(&k_full[gg % S], (gg / S) & 1, 2000000ull);
-          mbar_wait_drain(&v_full[gg % S], (gg / S) & 1, 2000000ull);
-        }
+        for (int u = max(0, n - NSL); u < n; ++u)
+          mbar_wait_drain(&kv_full[u % NSL], (u / NSL) & 1, 2000000ull);
       }
     }
     __syncwarp();
@@ -210,8 +198,8 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, false, false);
     constexpr uint32_t kIdO = idesc_bf16_f32(128, 256, false, true);
     const uint64_t qd = sdesc_sw128(sb + L::kQ, 16, 1024);
-    auto issue_s = [&](int buf, int st) {
-      const uint64_t kd = sdesc_sw128(sb + L::kK + st * L::kKVBytes, 16, 1024);
+    auto issue_s = [&](int buf, int sl) {
+      const uint64_t kd = sdesc_sw128(sb + L::kKV + sl * L::kKVBytes, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
         const uint32_t qoff = (kk >> 2) * L::kQSlab + (kk & 3) * 32;
@@ -220,35 +208,36 @@ __global__ void __launch_bounds__(320, 1)
                        kIdS, kk > 0 ? 1u : 0u);
       }
       mma_commit_if(leader, &s_full[buf]);
-      mma_commit_if(leader, &k_empty[st]);
+      mma_commit_if(leader, &kv_empty[sl]);
     };
-    auto issue_pv = [&](int buf, int st, bool first) {
+    auto issue_pv = [&](int buf, int sl, bool first) {
       // V is the MN-major B operand: 64-column slabs L::kKVSlab apart, 16 keys
       // (2048 bytes of 128-byte rows) per K step
-      const uint64_t vd = sdesc_sw128(sb + L::kV + st * L::kKVBytes, L::kKVSlab, 1024);
+      const uint64_t vd = sdesc_sw128(sb + L::kKV + sl * L::kKVBytes, L::kKVSlab, 1024);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_bf16_ts_if(leader, tmem + L::kTmemO, tmem + L::tmem_s(buf) + kk * 8,
                        sdesc_add(vd, kk * 2048), kIdO, (!first || kk > 0) ? 1u : 0u);
       mma_commit_if(leader, pv_done);
-      mma_commit_if(leader, &v_empty[st]);
+      mma_commit_if(leader, &kv_empty[sl]);
     };
     if (n_kv > 0) {
       mbar_wait(q_full, 0, wc, kSiteFwdQFull);
-      mbar_wait(&k_full[0], 0, wc, kSiteFwdKvFull);
+      mbar_wait(&kv_full[0], 0, wc, kSiteFwdKvFull);
       tc_fence_after();
       issue_s(0, 0);
       for (int j = 0; j < n_kv; ++j) {
         if (j + 1 < n_kv) {
-          const int g1 = j + 1;
-          mbar_wait(&k_full[g1 % S], (g1 / S) & 1, wc, kSiteFwdKvFull);
+          const int nk = 2 * (j + 1);  // ring item of K_{j+1}
+          mbar_wait(&kv_full[nk % NSL], (nk / NSL) & 1, wc, kSiteFwdKvFull);
           tc_fence_after();
-          issue_s(g1 & 1, g1 % S);
+          issue_s((j + 1) & 1, nk % NSL);
         }
+        const int nv = 2 * j + 1;  // ring item of V_j
         mbar_wait(&p_full[j & 1], (j >> 1) & 1, wc, kSiteFwdPFull);
-        mbar_wait(&v_full[j % S], (j / S) & 1, wc, kSiteFwdKvFull);
+        mbar_wait(&kv_full[nv % NSL], (nv / NSL) & 1, wc, kSiteFwdKvFull);
         tc_fence_after();
-        issue_pv(j & 1, j % S, j == 0);
+        issue_pv(j & 1, nv % NSL, j == 0);
       }
     }
     __syncwarp();
@@ -261,17 +250,18 @@ __global__ void __launch_bounds__(320, 1)
     float* red = reinterpret_cast<float*>(smem + L::kRed);
     const float sl2 = p.scale_log2;
     const PhiloxKey pk = DROPOUT ? launch_key(p.pk, p.rng_dev) : p.pk;
-    int xc = 0;  // exchanges; consecutive ones use alternate slots
+    // the half's value v, shared with the partner half through the pair's one
+    // slot: the first barrier makes sure the partner has read the previous
+    // value, the second that it has written this one
     auto exchange = [&](float v) {
-      float* slot = red + ((xc & 1) * 2) * 128;
-      ++xc;
-      slot[half * 128 + row] = v;
+      named_barrier_sync(pair_bar, 64);
+      red[half * 128 + row] = v;
       // also orders the partner's TMEM score reads before this warp's P
       // stores into the same columns
       tc_fence_before();
       named_barrier_sync(pair_bar, 64);
       tc_fence_after();
-      return slot[(1 - half) * 128 + row];
+      return red[(1 - half) * 128 + row];
     };
     const int b = it.b, h = it.h, bh = it.bh, q0 = it.q0, Sq = it.Sq, Sk = it.Sk, qs = it.qs;
     const int qi = q0 + row;
