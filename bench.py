@@ -78,6 +78,40 @@ def bwd_small_kernel_bytes(w):
     return pre + conv
 
 
+# Integer work of one Philox4x32-10 group (four keep decisions) as the
+# kernels draw it: ten rounds of two 32x32->64-bit products (the FMA pipe's
+# wide multiply) and two three-input XORs, then four threshold compares and
+# four selects. The forward takes each round's key from the kernel
+# parameters; the backward forms it at run time (two additions per round)
+# and assembles the quad's keep nibbles (about eight more operations).
+PHILOX_OPS = {"fwd": {"mul_wide": 20, "alu": 28}, "bwd": {"mul_wide": 20, "alu": 56}}
+# Per-SM integer rates used for the bound: the ALU pipe and the FMA pipe
+# (which executes the wide multiplies) each retire 64 lane-operations per
+# clock (16 lanes on each of the four schedulers); the two pipes run in
+# parallel, so the bound is the busier one.
+INT_LANE_OPS_PER_CLK_PER_SM = 64
+SM_COUNT = 152
+
+
+def philox_alu_bound(w, direction, clock_mhz, extra_ms):
+    """ALU roofline of the dropout draws of one pass: one group per four
+    visible (query, key) pairs (the keys past the causal diagonal are not
+    drawn), the pipe-bound time of its integer work at the sampled clock, and
+    the fraction of the pass's dropout time (the pass with p > 0 less the same
+    pass with p = 0) that bound accounts for."""
+    groups = pairs(w) * w.B * w.H / 4
+    ops = PHILOX_OPS[direction]
+    clk = (clock_mhz or 2070.0) * 1e6
+    per_pipe = {k: groups * n / (INT_LANE_OPS_PER_CLK_PER_SM * SM_COUNT * clk) * 1e3
+                for k, n in ops.items()}
+    bound = max(per_pipe.values())
+    return {"bound": "alu", "groups": groups, "ops_per_group": ops,
+            "lane_ops_per_clk_per_sm": INT_LANE_OPS_PER_CLK_PER_SM, "sm_count": SM_COUNT,
+            "clock_mhz": clock_mhz, "pipe_ms": per_pipe, "bound_ms": bound,
+            "dropout_extra_ms": extra_ms,
+            "frac": bound / extra_ms if extra_ms and extra_ms > 0 else None}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -612,7 +646,7 @@ def bench_ours(args, w):
     extras = None
     if not args.no_extras:
         extras = measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk, dv,
-                                ws, peak)
+                                ws, peak, t["fwd_ms"], t["bwd_ms"], clocks.get("sm_mhz"))
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(torch, sdpa, w, dev, stream, inputs_cpu, q, k, v, lse, ws, world)
@@ -631,7 +665,8 @@ def bench_ours(args, w):
     return 0
 
 
-def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk, dv, ws, peak):
+def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk, dv, ws, peak,
+                   base_fwd_ms, base_bwd_ms, clock_mhz):
     """The options entry points on the same workload, and the other named
     workloads' passes (each timed alone, CUDA events, mean of a few calls)."""
     extras = {}
@@ -680,8 +715,11 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
                                         out=out, lse=lse), 5)
     bwd_d = timed(lambda: sdpa.sdpa_bwd(do, q, k, v, out, lse, p_d, w.is_causal, w.seed,
                                         w.offset, None, dq=dq, dk=dk, dv=dv, workspace=ws), 5)
+    wd = W.make_workload(w.name, dropout_p=p_d)
     extras["dropout_0.1"] = _pass_line(w, fwd_d, bwd_d, "dropout_p 0.1 on the same B, H, S, D; "
                                        "the mask is regenerated in the backward", peak)
+    extras["dropout_0.1"]["alu_fwd"] = philox_alu_bound(wd, "fwd", clock_mhz, fwd_d - base_fwd_ms)
+    extras["dropout_0.1"]["alu_bwd"] = philox_alu_bound(wd, "bwd", clock_mhz, bwd_d - base_bwd_ms)
 
     # other head dims on the same B, H, S: 96 (the 128-wide kernels with the
     # last 32 columns zero-filled by TMA) and 256 (the 256-wide kernels)
@@ -749,7 +787,17 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
     # the other named workloads, each pass timed alone (inputs that fit in L2
     # get a 256 MB flush before every call, outside the events)
     for name in ("pages_test", "encoder_dropout", "cross_attn"):
-        extras[name] = measure_workload(torch, sdpa, W.WORKLOADS[name], dev, peak)
+        wl = W.WORKLOADS[name]
+        extras[name] = measure_workload(torch, sdpa, wl, dev, peak)
+        if wl.dropout_p > 0:
+            # the same pass without dropout: the dropout's own time
+            base = measure_workload(torch, sdpa, W.make_workload(name, dropout_p=0.0), dev, peak)
+            extras[name]["p0_fwd_ms"] = base["fwd_ms"]
+            extras[name]["p0_bwd_ms"] = base["bwd_ms"]
+            extras[name]["alu_fwd"] = philox_alu_bound(wl, "fwd", clock_mhz,
+                                                       extras[name]["fwd_ms"] - base["fwd_ms"])
+            extras[name]["alu_bwd"] = philox_alu_bound(wl, "bwd", clock_mhz,
+                                                       extras[name]["bwd_ms"] - base["bwd_ms"])
     if sdpa.sdpa_check_device() != 0:
         raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
     return extras

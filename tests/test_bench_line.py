@@ -91,3 +91,16 @@ def test_clock_window_keeps_only_its_samples_and_flags_throttling():
     assert c["reasons"] == ["sw_power_cap"] and c["rejected"] is False
     c2 = s.window(0.9, 3.0)
     assert c2["rejected"] is True and "hw_slowdown" in c2["reasons"]
+
+
+def test_philox_alu_bound_of_the_decoder_forward():
+    """One Philox group per four visible pairs; the bound is the busier of the
+    ALU and FMA pipes at 64 lane-operations per clock per SM."""
+    w = W.make_workload("decoder_long", dropout_p=0.1)
+    groups = 4096 * 4097 // 2 * 8 * 16 / 4
+    r = bench.philox_alu_bound(w, "fwd", 2000.0, 0.9)
+    assert r["groups"] == groups
+    alu_ms = groups * bench.PHILOX_OPS["fwd"]["alu"] / (64 * 152 * 2000e6) * 1e3
+    assert abs(r["bound_ms"] - alu_ms) < 1e-12  # 28 ALU ops per group outweigh 20 multiplies
+    assert abs(r["frac"] - alu_ms / 0.9) < 1e-12
+    assert bench.philox_alu_bound(w, "bwd", 2000.0, 0.0)["frac"] is None
