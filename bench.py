@@ -93,23 +93,30 @@ INT_LANE_OPS_PER_CLK_PER_SM = 64
 SM_COUNT = 152
 
 
-def philox_alu_bound(w, direction, clock_mhz, extra_ms):
-    """ALU roofline of the dropout draws of one pass: one group per four
-    visible (query, key) pairs (the keys past the causal diagonal are not
-    drawn), the pipe-bound time of its integer work at the sampled clock, and
-    the fraction of the pass's dropout time (the pass with p > 0 less the same
-    pass with p = 0) that bound accounts for."""
+def philox_alu_bound(w, direction, clock_mhz, pass_ms, base_ms, peak_tflops):
+    """Roofline of one pass with dropout, which has two bounds: its tensor
+    work (the pass's algorithmic flops at the dense bf16 peak) and the integer
+    work of its dropout draws -- one Philox group per four visible (query,
+    key) pairs (keys past the causal diagonal are not drawn), timed on the
+    busier of the ALU and FMA pipes at the sampled clock. The two run on
+    different units and overlap, so the pass can be no faster than the larger
+    bound; frac = that bound / the measured pass. dropout_extra_ms, the pass
+    less the same pass at p = 0, is the time the draws did not hide."""
     groups = pairs(w) * w.B * w.H / 4
     ops = PHILOX_OPS[direction]
     clk = (clock_mhz or 2070.0) * 1e6
     per_pipe = {k: groups * n / (INT_LANE_OPS_PER_CLK_PER_SM * SM_COUNT * clk) * 1e3
                 for k, n in ops.items()}
-    bound = max(per_pipe.values())
-    return {"bound": "alu", "groups": groups, "ops_per_group": ops,
-            "lane_ops_per_clk_per_sm": INT_LANE_OPS_PER_CLK_PER_SM, "sm_count": SM_COUNT,
-            "clock_mhz": clock_mhz, "pipe_ms": per_pipe, "bound_ms": bound,
-            "dropout_extra_ms": extra_ms,
-            "frac": bound / extra_ms if extra_ms and extra_ms > 0 else None}
+    alu_ms = max(per_pipe.values())
+    f_fwd, f_bwd = flops(w)
+    tensor_ms = (f_fwd if direction == "fwd" else f_bwd) / (peak_tflops * 1e12) * 1e3
+    bound = max(alu_ms, tensor_ms)
+    return {"bound": "alu" if alu_ms >= tensor_ms else "tensor", "groups": groups,
+            "ops_per_group": ops, "lane_ops_per_clk_per_sm": INT_LANE_OPS_PER_CLK_PER_SM,
+            "sm_count": SM_COUNT, "clock_mhz": clock_mhz, "pipe_ms": per_pipe,
+            "alu_bound_ms": alu_ms, "tensor_bound_ms": tensor_ms, "pass_ms": pass_ms,
+            "frac": bound / pass_ms if pass_ms > 0 else None,
+            "dropout_extra_ms": pass_ms - base_ms}
 
 
 def peaks():
@@ -718,8 +725,10 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
     wd = W.make_workload(w.name, dropout_p=p_d)
     extras["dropout_0.1"] = _pass_line(w, fwd_d, bwd_d, "dropout_p 0.1 on the same B, H, S, D; "
                                        "the mask is regenerated in the backward", peak)
-    extras["dropout_0.1"]["alu_fwd"] = philox_alu_bound(wd, "fwd", clock_mhz, fwd_d - base_fwd_ms)
-    extras["dropout_0.1"]["alu_bwd"] = philox_alu_bound(wd, "bwd", clock_mhz, bwd_d - base_bwd_ms)
+    extras["dropout_0.1"]["alu_fwd"] = philox_alu_bound(wd, "fwd", clock_mhz, fwd_d, base_fwd_ms,
+                                                        peak)
+    extras["dropout_0.1"]["alu_bwd"] = philox_alu_bound(wd, "bwd", clock_mhz, bwd_d, base_bwd_ms,
+                                                        peak)
 
     # other head dims on the same B, H, S: 96 (the 128-wide kernels with the
     # last 32 columns zero-filled by TMA) and 256 (the 256-wide kernels)
@@ -794,10 +803,10 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
             base = measure_workload(torch, sdpa, W.make_workload(name, dropout_p=0.0), dev, peak)
             extras[name]["p0_fwd_ms"] = base["fwd_ms"]
             extras[name]["p0_bwd_ms"] = base["bwd_ms"]
-            extras[name]["alu_fwd"] = philox_alu_bound(wl, "fwd", clock_mhz,
-                                                       extras[name]["fwd_ms"] - base["fwd_ms"])
-            extras[name]["alu_bwd"] = philox_alu_bound(wl, "bwd", clock_mhz,
-                                                       extras[name]["bwd_ms"] - base["bwd_ms"])
+            extras[name]["alu_fwd"] = philox_alu_bound(wl, "fwd", clock_mhz, extras[name]["fwd_ms"],
+                                                       base["fwd_ms"], peak)
+            extras[name]["alu_bwd"] = philox_alu_bound(wl, "bwd", clock_mhz, extras[name]["bwd_ms"],
+                                                       base["bwd_ms"], peak)
     if sdpa.sdpa_check_device() != 0:
         raise RuntimeError("kernel wait timed out in the extended-entry-point timings")
     return extras

@@ -94,13 +94,16 @@ def test_clock_window_keeps_only_its_samples_and_flags_throttling():
 
 
 def test_philox_alu_bound_of_the_decoder_forward():
-    """One Philox group per four visible pairs; the bound is the busier of the
-    ALU and FMA pipes at 64 lane-operations per clock per SM."""
+    """One Philox group per four visible pairs; the ALU bound is the busier of
+    the ALU and FMA pipes at 64 lane-operations per clock per SM, and the
+    pass's roofline the larger of that and its tensor bound."""
     w = W.make_workload("decoder_long", dropout_p=0.1)
     groups = 4096 * 4097 // 2 * 8 * 16 / 4
-    r = bench.philox_alu_bound(w, "fwd", 2000.0, 0.9)
+    r = bench.philox_alu_bound(w, "fwd", 2000.0, 1.35, 0.41, 1940.8)
     assert r["groups"] == groups
     alu_ms = groups * bench.PHILOX_OPS["fwd"]["alu"] / (64 * 152 * 2000e6) * 1e3
-    assert abs(r["bound_ms"] - alu_ms) < 1e-12  # 28 ALU ops per group outweigh 20 multiplies
-    assert abs(r["frac"] - alu_ms / 0.9) < 1e-12
-    assert bench.philox_alu_bound(w, "bwd", 2000.0, 0.0)["frac"] is None
+    assert abs(r["alu_bound_ms"] - alu_ms) < 1e-12  # 28 ALU ops per group outweigh 20 multiplies
+    tensor_ms = bench.flops(w)[0] / 1940.8e12 * 1e3
+    assert abs(r["tensor_bound_ms"] - tensor_ms) < 1e-12
+    assert r["bound"] == "alu" and abs(r["frac"] - max(alu_ms, tensor_ms) / 1.35) < 1e-12
+    assert abs(r["dropout_extra_ms"] - 0.94) < 1e-12
