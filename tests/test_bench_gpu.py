@@ -35,4 +35,4 @@ def test_default_bench_path_prints_a_complete_line(cuda_lib):
                  "head_dim_96", "head_dim_256", "pages_test", "encoder_dropout", "cross_attn"):
         assert name in line["extended"], name
     for name in ("dropout_0.1", "encoder_dropout", "cross_attn"):
-        assert line["extended"][name]["alu_fwd"]["bound_ms"] > 0, name
+        assert line["extended"][name]["alu_fwd"]["alu_bound_ms"] > 0, name
