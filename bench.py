@@ -574,11 +574,15 @@ def bench_ours(args, w):
     ws = torch.empty(sdpa.sdpa_bwd_workspace_size(w.B, w.H, w.Sq, w.Sk, w.D), dtype=torch.uint8,
                      device=dev)
     stream = torch.cuda.current_stream(dev)
+    # profiling the bias path: a relative-position bias shared by the batch
+    bias = (W.padded_rows(W.draw_bias((1, w.H, w.Sq, w.Sk), w.input_seed + 17, "relpos").to(dev))
+            if args.bias else None)
 
     def step():
-        sdpa.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset, out=out, lse=lse)
-        sdpa.sdpa_bwd(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
-                      dq=dq, dk=dk, dv=dv, workspace=ws)
+        sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset,
+                         attn_bias=bias, out=out, lse=lse)
+        sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
+                         attn_bias=bias, dq=dq, dk=dk, dv=dv, workspace=ws)
 
     warmup = max(args.warmup, 3)
     for _ in range(warmup):
@@ -613,10 +617,11 @@ def bench_ours(args, w):
             flush.fill_(float(i))
         ev[i][0].record(stream)
         sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset, out=out,
-                         lse=lse, kernel_events=km[i][0:2])
+                         lse=lse, attn_bias=bias, kernel_events=km[i][0:2])
         ev[i][1].record(stream)
         sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
-                         dq=dq, dk=dk, dv=dv, workspace=ws, kernel_events=km[i][2:4])
+                         attn_bias=bias, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         kernel_events=km[i][2:4])
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -668,6 +673,8 @@ def bench_ours(args, w):
                "sample": f"{heads} whole heads of {w.B * w.H} (fwd+bwd, fp64 numpy, {el:.1f} s)"}
     line = assemble_line(w, world, args.steps, warmup, t, pk_table, pk_src, clocks, sustained,
                          extras, e2e, cpu)
+    if bias is not None:
+        line["config"]["bias"] = "relative-position [1, H, Sq, Sk] bf16 (profiling case)"
     print(json.dumps(line))
     return 0
 
@@ -950,6 +957,11 @@ def main(argv=None):
                     help="override B (small cases for profiling; not a bench line)")
     ap.add_argument("--dropout", type=float, default=None,
                     help="override dropout_p (profiling the dropout path; not a bench line)")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="override D (profiling other head dims; not a bench line)")
+    ap.add_argument("--bias", choices=["relpos"], default=None,
+                    help="add a relative-position bias [1, H, Sq, Sk] to every call (profiling "
+                         "the bias path; not a bench line)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another named workload of the package's workloads module (its own "
                          "shape; the bench line is the default one)")
@@ -961,6 +973,8 @@ def main(argv=None):
         over["B"] = args.batch
     if args.dropout is not None:
         over["dropout_p"] = args.dropout
+    if args.head_dim is not None:
+        over["D"] = args.head_dim
     if over:
         w = W.make_workload(args.workload, **over)
     if args.impl == "reference":
