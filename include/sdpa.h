@@ -212,6 +212,24 @@ sdpa_status sdpa_dropout_mask_debug(int64_t B, int64_t H, int64_t Sq, int64_t Sk
  *     the tiles finish). It needs the larger workspace that
  *     sdpa_bwd_workspace_size_ex() reports and moves about twice the partials'
  *     bytes through HBM.
+ *   dropout_bits, dropout_bits_bytes: NULL, or a device buffer (4-byte
+ *     aligned, at least sdpa_dropout_bits_size(B, H, Sq, Sk) bytes) that
+ *     carries the dropout keep mask from the forward to the backward. With
+ *     dropout_p > 0, sdpa_fwd_ex writes into it the keep bits of every score
+ *     tile it computes, and sdpa_bwd_ex, given the same buffer, reads them
+ *     instead of drawing them again: the same mask (both sides draw it from
+ *     the absolute index, "REDO of dropout support for mem eff #102038",
+ *     pytorch PR 103704), so the same results, with the backward's Philox
+ *     work replaced by 1/8 byte per score read from device memory. The
+ *     backward trusts the buffer: it must be the one the forward filled for
+ *     the same B, H, Sq, Sk, dropout_p, seed and offset (or rng_state values)
+ *     and batch / head position, unchanged since. Layout: uint32 word
+ *     ((b*H + h)*ceil128(Sk)/32 + w)*ceil128(Sq) + i holds the keep bits of
+ *     keys 32w .. 32w+31 of query row i (bit e: key 32w+e kept); words of
+ *     tiles the causal mask skips are not written. Ignored when dropout_p
+ *     is 0. Head dims up to 128 only, without attn_bias and without a packed
+ *     batch (else SDPA_ERR_UNSUPPORTED); a short buffer is
+ *     SDPA_ERR_INVALID_ARG, a misaligned one SDPA_ERR_ALIGNMENT.
  *   kernel_events: NULL, or a pointer to two cudaEvent_t handles that the
  *     call records on `stream` immediately before and after its main kernel:
  *     the forward kernel, or the backward's main kernel (between its
@@ -231,7 +249,14 @@ typedef struct {
   const sdpa_tensor* attn_bias;
   sdpa_tensor* dbias;
   void* const* kernel_events;
+  uint32_t* dropout_bits;
+  size_t dropout_bits_bytes;
 } sdpa_options;
+
+/* Bytes of the dropout_bits buffer of a [B, H, Sq, Sk] problem:
+ * B*H*ceil128(Sq)*ceil128(Sk)/8 (0 for an empty problem or negative sizes,
+ * SIZE_MAX when it does not fit in 62 bits). */
+size_t sdpa_dropout_bits_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk);
 
 /* sdpa_fwd with options (NULL options = sdpa_fwd). */
 sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,

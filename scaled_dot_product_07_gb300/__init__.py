@@ -28,6 +28,7 @@ __all__ = [
     "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "sdpa_fwd_ex", "sdpa_bwd_ex",
     "sdpa_bwd_workspace_size_ex", "sdpa_dropout_mask_debug_ex", "SdpaOptions",
     "sdpa_fwd_varlen", "sdpa_bwd_varlen", "sdpa_bwd_varlen_workspace_size", "SdpaVarlen",
+    "sdpa_dropout_bits_size",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -39,7 +40,7 @@ EXPORTED_SYMBOLS = (
     "sdpa_fwd", "sdpa_bwd_workspace_size", "sdpa_bwd", "sdpa_dropout_mask_debug",
     "sdpa_check_device", "sdpa_selftest_wait_timeout", "sdpa_status_string", "sdpa_bwd_noalloc",
     "sdpa_fwd_ex", "sdpa_bwd_workspace_size_ex", "sdpa_bwd_ex", "sdpa_dropout_mask_debug_ex",
-    "sdpa_fwd_varlen", "sdpa_bwd_varlen_workspace_size", "sdpa_bwd_varlen",
+    "sdpa_fwd_varlen", "sdpa_bwd_varlen_workspace_size", "sdpa_bwd_varlen", "sdpa_dropout_bits_size",
 )
 
 # SDPA_BWD_NOALLOC_SCRATCH_BYTES of include/sdpa.h
@@ -76,7 +77,8 @@ class SdpaOptions(ctypes.Structure):
     _fields_ = [("rng_state", ctypes.c_void_p), ("batch_offset", ctypes.c_int64),
                 ("head_offset", ctypes.c_int64), ("total_heads", ctypes.c_int64),
                 ("deterministic", ctypes.c_int), ("attn_bias", ctypes.c_void_p),
-                ("dbias", ctypes.c_void_p), ("kernel_events", ctypes.c_void_p)]
+                ("dbias", ctypes.c_void_p), ("kernel_events", ctypes.c_void_p),
+                ("dropout_bits", ctypes.c_void_p), ("dropout_bits_bytes", ctypes.c_size_t)]
 
 
 def library_path():
@@ -124,6 +126,8 @@ def load_library(path=None):
     lib.sdpa_bwd_varlen.argtypes = [P, P, P, P, P, vp, vp, dbl, ctypes.c_int, u64, u64, flt, P, P,
                                     P, vp, ctypes.c_size_t, vp, vp]
     lib.sdpa_bwd_varlen.restype = ctypes.c_int
+    lib.sdpa_dropout_bits_size.argtypes = [i64, i64, i64, i64]
+    lib.sdpa_dropout_bits_size.restype = ctypes.c_size_t
     lib.sdpa_check_device.argtypes = [vp]
     lib.sdpa_check_device.restype = ctypes.c_int
     lib.sdpa_selftest_wait_timeout.argtypes = [u64, vp]
@@ -295,14 +299,21 @@ def _event_handle(e):
 
 
 def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deterministic=False,
-             attn_bias=None, dbias=None, kernel_events=None):
+             attn_bias=None, dbias=None, kernel_events=None, dropout_bits=None):
     """sdpa_options (by pointer) for the *_ex calls; rng_state is a device
     tensor holding {seed, offset} as two 64-bit integers, or None; attn_bias
     and dbias are bfloat16 tensors or None; kernel_events is None or a pair of
     torch.cuda.Event (timing enabled, each recorded once already) that the
-    library records around the call's main kernel."""
+    library records around the call's main kernel; dropout_bits is None or a
+    contiguous CUDA tensor of sdpa_dropout_bits_size() bytes that carries the
+    dropout keep mask from the forward to the backward."""
     o = SdpaOptions()
     o._keep = []
+    if dropout_bits is not None:
+        if not dropout_bits.is_cuda or not dropout_bits.is_contiguous():
+            raise ValueError("dropout_bits must be a contiguous CUDA tensor")
+        o.dropout_bits = dropout_bits.data_ptr()
+        o.dropout_bits_bytes = dropout_bits.numel() * dropout_bits.element_size()
     if kernel_events is not None:
         a, b = kernel_events
         handles = (ctypes.c_void_p * 2)(_event_handle(a), _event_handle(b))
@@ -327,15 +338,24 @@ def _options(rng_state=None, batch_offset=0, head_offset=0, total_heads=0, deter
     return o
 
 
+def sdpa_dropout_bits_size(B, H, Sq, Sk):
+    """Bytes of the buffer that carries the dropout keep bits of a [B, H, Sq,
+    Sk] problem from the forward to the backward (``dropout_bits``)."""
+    return int(load_library().sdpa_dropout_bits_size(B, H, Sq, Sk))
+
+
 def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, offset=0,
                 rng_state=None, batch_offset=0, head_offset=0, total_heads=0, attn_bias=None,
-                out=None, lse=None, kernel_events=None):
+                out=None, lse=None, kernel_events=None, dropout_bits=None):
     """Forward with options: ``rng_state`` (device {seed, offset}, read by the
     kernels when they run, e.g. inside a replayed CUDA graph), the batch /
     head position of this call in a larger split problem, an additive
-    bfloat16 ``attn_bias`` [B or 1, H or 1, Sq, Sk] of the scaled scores, and
+    bfloat16 ``attn_bias`` [B or 1, H or 1, Sq, Sk] of the scaled scores,
     ``kernel_events`` (a pair of torch.cuda.Event recorded around the forward
-    kernel, for timing it alone). Returns (out, lse)."""
+    kernel, for timing it alone) and ``dropout_bits`` (a device buffer of
+    :func:`sdpa_dropout_bits_size` bytes into which the forward writes its
+    dropout keep bits, for a backward given the same buffer). Returns (out,
+    lse)."""
     import torch
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -344,7 +364,7 @@ def sdpa_fwd_ex(q, k, v, dropout_p=0.0, is_causal=False, scale=None, seed=0, off
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if lse is None else lse
     opt = _options(rng_state, batch_offset, head_offset, total_heads, attn_bias=attn_bias,
-                   kernel_events=kernel_events)
+                   kernel_events=kernel_events, dropout_bits=dropout_bits)
     dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.sdpa_fwd_ex(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), float(dropout_p),
                          int(bool(is_causal)), _default_scale(D, scale), int(seed), int(offset),
@@ -362,11 +382,13 @@ def sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, deterministic=False):
 def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0, offset=0,
                 scale=None, rng_state=None, batch_offset=0, head_offset=0, total_heads=0,
                 deterministic=False, attn_bias=None, dbias=None, dq=None, dk=None, dv=None,
-                workspace=None, kernel_events=None):
+                workspace=None, kernel_events=None, dropout_bits=None):
     """Backward with options (see :func:`sdpa_fwd_ex`); ``deterministic``
     selects the fixed-order dQ accumulation. ``dbias``: None, True (allocate)
     or a bfloat16 [B, H, Sq, Sk] tensor that receives the bias gradient dS.
     ``kernel_events`` are recorded around the backward's main kernel.
+    ``dropout_bits``: the buffer a forward of the same problem filled; the
+    backward reads the keep bits from it instead of drawing them.
     Returns (dq, dk, dv), or (dq, dk, dv, dbias) when dbias is requested."""
     import torch
     lib = load_library()
@@ -382,7 +404,7 @@ def sdpa_bwd_ex(dout, q, k, v, out, lse, dropout_p=0.0, is_causal=False, seed=0,
         pad = (Sk + 7) // 8 * 8
         dbias = torch.empty((B, H, Sq, pad), dtype=torch.bfloat16, device=q.device)[..., :Sk]
     opt = _options(rng_state, batch_offset, head_offset, total_heads, deterministic, attn_bias,
-                   dbias, kernel_events)
+                   dbias, kernel_events, dropout_bits)
     need = int(lib.sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, ctypes.byref(opt)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

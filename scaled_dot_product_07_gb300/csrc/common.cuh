@@ -69,6 +69,10 @@ struct FwdParams {
   const int32_t* cu_k;
   int Sq_ctr, Sk_ctr;       // dims of the dropout counter (Sq, Sk; or the max lengths)
   int total_q;              // packed query rows (lse is [H, total_q] when packed)
+  // dropout keep bits stored for the backward (null: not stored): word
+  // (bh*bits_kw + w)*bits_rows + i holds keys 32w .. 32w+31 of row i
+  uint32_t* drop_bits;
+  int64_t bits_kw, bits_rows;
   int D_io;                 // the caller's head dim (columns of out)
   StridedBf16 out_io;       // out, for the direct stores of a sequence's last tile
   float* lse;             // [B, H, Sq] fp32
@@ -93,6 +97,10 @@ struct BwdParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int Sq_ctr, Sk_ctr;       // dims of the dropout counter
+  // dropout keep bits the forward stored (null: drawn here), laid out as in
+  // FwdParams
+  const uint32_t* drop_bits;
+  int64_t bits_kw, bits_rows;
   int D_io;                 // the caller's head dim (columns of dk, dv)
   StridedBf16 dk_io, dv_io; // for the direct stores of a sequence's last key tile
   StridedBf16 k_io;         // k, read row by row by the 256-wide kernel (K into TMEM)

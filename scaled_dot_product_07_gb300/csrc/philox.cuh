@@ -89,6 +89,40 @@ __device__ __forceinline__ uint4 philox_group_rk(uint64_t g, uint32_t off_lo, ui
   return make_uint4(c0, c1, c2, c3);
 }
 
+// 32 x 32 bit transpose across a warp: lane l passes row l (bit c = column
+// c) and gets column l back (bit r = row r). Five butterfly stages; in the
+// stage of distance s each lane keeps its own half of every 2s-bit block
+// and takes the matching half from lane l ^ s. All 32 lanes must call it.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  const uint32_t masks[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    const int s = 16 >> i;
+    const uint32_t m = masks[i];
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+    x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+  }
+  return x;
+}
+
+// Keep bits of the 16 groups g0 .. g0+15 (elements 4 g0 .. 4 g0 + 63): bit
+// 4t + w of words[t / 8] (t mod 8 in place of t) is 1 iff element
+// 4(g0 + t) + w is kept. RK: the round keys the host formed (rk); else
+// formed from pk.
+template <bool RK>
+__device__ __forceinline__ void keep_words_aligned(uint64_t g0, uint32_t threshold,
+                                                   const PhiloxKey& pk, const PhiloxRoundKeys& rk,
+                                                   uint32_t (&words)[2]) {
+  words[0] = words[1] = 0u;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const uint4 u = RK ? philox_group_rk(g0 + t, pk.off_lo, pk.off_hi, rk) : philox_group(g0 + t, pk);
+    const uint32_t nib = (u.x >= threshold ? 1u : 0u) | (u.y >= threshold ? 2u : 0u) |
+                         (u.z >= threshold ? 4u : 0u) | (u.w >= threshold ? 8u : 0u);
+    words[t >> 3] |= nib << (4 * (t & 7));
+  }
+}
+
 // Keep bits of the 32*W consecutive absolute indices n0 .. n0+32W-1:
 // bit e of bits[e/32] is 1 iff element n0+e is kept.
 template <int W>

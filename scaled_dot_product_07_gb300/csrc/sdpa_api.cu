@@ -265,6 +265,7 @@ struct Opts {
   int64_t bias_B = 0, bias_H = 0;  // the bias's own batch and head extents (1 when shared)
   DBias dbias{nullptr, 0, 0, 0};
   cudaEvent_t ev_begin = nullptr, ev_end = nullptr;  // around the main kernel
+  uint32_t* bits = nullptr;  // dropout keep bits carried from forward to backward
 };
 
 // Records one of the caller's kernel events (none when it is null).
@@ -348,6 +349,11 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
       x.ev_end = static_cast<cudaEvent_t>(o->kernel_events[1]);
       if (!x.ev_begin || !x.ev_end) return SDPA_ERR_INVALID_ARG;
     }
+    if (o->dropout_bits) {
+      if (reinterpret_cast<uintptr_t>(o->dropout_bits) & 3u) return SDPA_ERR_ALIGNMENT;
+      if (o->dropout_bits_bytes < sdpa_dropout_bits_size(B, H, Sq, Sk)) return SDPA_ERR_INVALID_ARG;
+      x.bits = o->dropout_bits;
+    }
     x.rng = o->rng_state;
     x.b0 = static_cast<int>(o->batch_offset);
     x.h0 = static_cast<int>(o->head_offset);
@@ -355,6 +361,14 @@ sdpa_status resolve_options(const sdpa_options* o, int64_t B, int64_t H, int64_t
     x.det = o->deterministic != 0;
   }
   *r = x;
+  return SDPA_OK;
+}
+
+// Stored dropout bits serve the 128-wide kernels of one [Sq, Sk] problem per
+// (batch, head): not the 256-wide ones, a bias or a packed batch.
+sdpa_status check_bits(const Opts& opt, int64_t D, double dropout_p, bool packed) {
+  if (opt.bits == nullptr || !(dropout_p > 0.0)) return SDPA_OK;
+  if (D > 128 || opt.bias.data != nullptr || packed) return SDPA_ERR_UNSUPPORTED;
   return SDPA_OK;
 }
 
@@ -420,6 +434,11 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
   p.Sq_ctr = static_cast<int>(Sq);
   p.Sk_ctr = static_cast<int>(Sk);
   p.total_q = static_cast<int>(total_q);
+  p.drop_bits = dropout_p > 0.0 ? opt.bits : nullptr;
+  p.bits_kw = round_up(Sk, 128) / 32;
+  p.bits_rows = round_up(Sq, 128);
+  if (p.drop_bits != nullptr && (Dk == 256 || opt.bias.data != nullptr || cu_q != nullptr))
+    return SDPA_ERR_UNSUPPORTED;
   p.D_io = static_cast<int>(D);
   p.out_io = strided(out);
   p.lse = lse;
@@ -447,6 +466,9 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
                        const sdpa_options* options, const Opts& opt, const int32_t* cu_q,
                        const int32_t* cu_k, int64_t total_q, cudaStream_t stream) {
   const int64_t Dk = bwd_kernel_head_dim(D);
+  if (dropout_p > 0.0 && opt.bits != nullptr &&
+      (Dk == 256 || opt.bias.data != nullptr || cu_q != nullptr))
+    return SDPA_ERR_UNSUPPORTED;
   const size_t need = sdpa_bwd_workspace_size_ex(B, H, Sq, Sk, D, options);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SDPA_ERR_WORKSPACE;
@@ -524,6 +546,9 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   p.cu_k = cu_k;
   p.Sq_ctr = static_cast<int>(Sq);
   p.Sk_ctr = static_cast<int>(Sk);
+  p.drop_bits = dropout_p > 0.0 ? opt.bits : nullptr;
+  p.bits_kw = round_up(Sk, 128) / 32;
+  p.bits_rows = round_up(Sq, 128);
   p.D_io = static_cast<int>(D);
   p.dk_io = strided(dk);
   p.dv_io = strided(dv);
@@ -606,6 +631,7 @@ sdpa_status sdpa_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_t
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
   Opts opt;
   if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
+  if ((s = check_bits(opt, D, dropout_p, false)) != SDPA_OK) return s;
   return fwd_launch(q, k, v, out, lse, B, H, Sq, Sk, D, dropout_p, is_causal, scale, seed, offset,
                     opt, nullptr, nullptr, 0, stream);
 }
@@ -631,6 +657,7 @@ sdpa_status sdpa_fwd_varlen(const sdpa_tensor* q, const sdpa_tensor* k, const sd
   const int64_t B = seqs->batch, Mq = seqs->max_seqlen_q, Mk = seqs->max_seqlen_k;
   Opts opt;
   if ((s = resolve_options(options, B, H, Mq, Mk, &opt)) != SDPA_OK) return s;
+  if ((s = check_bits(opt, D, dropout_p, true)) != SDPA_OK) return s;
   return fwd_launch(q, k, v, out, lse, B, H, Mq, Mk, D, dropout_p, is_causal, scale, seed, offset,
                     opt, seqs->cu_seqlens_q, seqs->cu_seqlens_k, Tq, stream);
 }
@@ -646,6 +673,16 @@ size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
   return checked_bytes(B, H, round_up(Sq, 128), bwd_kernel_head_dim(D) + 2);
+}
+
+size_t sdpa_dropout_bits_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk) {
+  if (B <= 0 || H <= 0 || Sq <= 0 || Sk <= 0) return 0;
+  // B*H*ceil128(Sq)*ceil128(Sk)/8 bytes = B*H*ceil128(Sq) rows of ceil128(Sk)/32 words
+  const double bytes = static_cast<double>(B) * static_cast<double>(H) *
+                       static_cast<double>(round_up(Sq, 128)) * static_cast<double>(round_up(Sk, 128)) / 8.0;
+  if (bytes > 4.0e18) return SIZE_MAX;
+  return static_cast<size_t>(B) * static_cast<size_t>(H) * static_cast<size_t>(round_up(Sq, 128)) *
+         static_cast<size_t>(round_up(Sk, 128) / 32) * 4u;
 }
 
 size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
@@ -687,6 +724,7 @@ sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdp
   if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SDPA_ERR_INVALID_ARG;
   Opts opt;
   if ((s = resolve_options(options, B, H, Sq, Sk, &opt)) != SDPA_OK) return s;
+  if ((s = check_bits(opt, D, dropout_p, false)) != SDPA_OK) return s;
   return bwd_launch(dout, q, k, v, out, lse, B, H, Sq, Sk, D, dropout_p, is_causal, seed, offset,
                     scale, dq, dk, dv, workspace, workspace_bytes, options, opt, nullptr, nullptr, 0,
                     stream);
@@ -736,6 +774,7 @@ sdpa_status sdpa_bwd_varlen(const sdpa_tensor* dout, const sdpa_tensor* q, const
   const int64_t B = seqs->batch, Mq = seqs->max_seqlen_q, Mk = seqs->max_seqlen_k;
   Opts opt;
   if ((s = resolve_options(options, B, H, Mq, Mk, &opt)) != SDPA_OK) return s;
+  if ((s = check_bits(opt, D, dropout_p, true)) != SDPA_OK) return s;
   return bwd_launch(dout, q, k, v, out, lse, B, H, Mq, Mk, D, dropout_p, is_causal, seed, offset,
                     scale, dq, dk, dv, workspace, workspace_bytes, options, opt,
                     seqs->cu_seqlens_q, seqs->cu_seqlens_k, Tq, stream);

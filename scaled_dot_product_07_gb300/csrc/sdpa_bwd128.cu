@@ -333,7 +333,17 @@ __global__ void __launch_bounds__(448, 1)
       // the step's dropout keep bits depend only on the indices: drawn while
       // the tensor core computes S^T
       uint32_t kb[2] = {0xffffffffu, 0xffffffffu};
-      if (DROPOUT) {
+      // with the forward's stored bits: lane l reads rows i0 + l and i0 + 32 + l
+      // of its warp's 32 keys (transposed to one word per key after the waits)
+      const bool stored = DROPOUT && !BIAS && !VARLEN && p.drop_bits != nullptr;
+      uint32_t sw[2] = {0u, 0u};
+      if (stored) {
+        const uint32_t* wp =
+            p.drop_bits + (static_cast<size_t>(bh) * p.bits_kw + (k0 >> 5) + (warp & 3)) * p.bits_rows +
+            i0 + lane;
+        sw[0] = wp[0];
+        sw[1] = wp[32];
+      } else if (DROPOUT) {
         const uint64_t n_base = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + i0) *
                                     static_cast<uint64_t>(p.Sk_ctr) +
                                 kj;
@@ -351,6 +361,10 @@ __global__ void __launch_bounds__(448, 1)
       mbar_wait_t<kInlineWaits>(&q_full[st], (t / NS) & 1, wc, kSiteBwdQFull);
       mbar_wait_t<kInlineWaits>(&s_full[x], k & 1, wc, kSiteBwdSFull);
       tc_fence_after();
+      if (stored) {
+        kb[0] = warp_transpose32(sw[0], lane);
+        kb[1] = warp_transpose32(sw[1], lane);
+      }
       float pv[MQ];
       {
         uint32_t r0[32], r1[32];

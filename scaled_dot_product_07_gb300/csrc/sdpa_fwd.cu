@@ -157,7 +157,10 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
   return it;
 }
 
-template <int D, bool CAUSAL, bool DROPOUT, bool VARLEN>
+// STORE (with DROPOUT, not VARLEN): the keep bits are also written to
+// p.drop_bits for the backward. It is a separate instantiation so that the
+// plain dropout kernel keeps its registers.
+template <int D, bool CAUSAL, bool DROPOUT, bool VARLEN, bool STORE = false>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v,
@@ -437,7 +440,9 @@ __global__ void __launch_bounds__(320, 1)
             const float alpha = ex2_approx((m[i] - m_new) * sl2);
             l[i] *= alpha;
             m[i] = m_new;
-  #pragma unroll
+            // (not unrolled: the branch is rare, and two chunks of O live
+            // beside the scores made the kernel spill registers)
+  #pragma unroll 1
             for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
               uint32_t o[32];
               tmem_ld32(tO + (D / 2) * half + c * 32, o);
@@ -491,14 +496,36 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t n0 = (counter_bh(b, h, p.b0, p.h0, p.H_total) * p.Sq_ctr + qi) *
                                     static_cast<uint64_t>(p.Sk_ctr) +
                                 k0;
+            // STORE: kept for the backward, words k0/32 and k0/32 + 1 of row qi
+            uint32_t* wp = STORE ? p.drop_bits +
+                                       (static_cast<size_t>(bh) * p.bits_kw + (k0 >> 5)) * p.bits_rows +
+                                       qi
+                                 : nullptr;
             if ((p.Sk_ctr & 3) == 0) {
-              if (p.rng_dev == nullptr)
-                exp_pack(std::integral_constant<int, 1>{}, n0 >> 2, no_bits);
-              else
-                exp_pack(std::integral_constant<int, 3>{}, n0 >> 2, no_bits);
+              if constexpr (STORE) {
+                // the half row's 16 groups first (group t: keys 4t .. 4t+3),
+                // stored, then applied from the bits
+                uint32_t keep[2];
+                if (p.rng_dev == nullptr)
+                  keep_words_aligned<true>(n0 >> 2, p.drop_threshold, p.pk, p.rk, keep);
+                else
+                  keep_words_aligned<false>(n0 >> 2, p.drop_threshold, pk, p.rk, keep);
+                wp[0] = keep[0];
+                wp[p.bits_rows] = keep[1];
+                exp_pack(std::integral_constant<int, 2>{}, 0, keep);
+              } else {
+                if (p.rng_dev == nullptr)
+                  exp_pack(std::integral_constant<int, 1>{}, n0 >> 2, no_bits);
+                else
+                  exp_pack(std::integral_constant<int, 3>{}, n0 >> 2, no_bits);
+              }
             } else {
               uint32_t keep[2];
               keep_bits<2>(n0, p.drop_threshold, pk, keep);
+              if (STORE) {
+                wp[0] = keep[0];
+                wp[p.bits_rows] = keep[1];
+              }
               exp_pack(std::integral_constant<int, 2>{}, 0, keep);
             }
           }
@@ -976,11 +1003,11 @@ __global__ void __launch_bounds__(320, 1)
 
 
 // Two items per CTA once there are more than two items per SM, else one.
-template <int D, bool C, bool DR, bool VL>
+template <int D, bool C, bool DR, bool VL, bool ST = false>
 cudaError_t launch_fwd_t(const CUtensorMap* maps, const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<D, C, DR, VL>;
+  auto kern = fwd_kernel<D, C, DR, VL, ST>;
   const int smem = FwdLayout<D>::kAlloc;
-  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, VL>>(smem);
+  cudaError_t e = ensure_smem_attr<fwd_kernel<D, C, DR, VL, ST>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
   FwdParams pl = p;
@@ -1008,11 +1035,15 @@ cudaError_t launch_fwd(int D, bool causal, bool dropout, const CUtensorMap* maps
                        const FwdParams& p, cudaStream_t stream) {
   const bool bias = p.bias.data != nullptr;
   const bool varlen = p.cu_q != nullptr;  // packed batches take no bias
+  // the keep bits are stored (dropout only; the host allows no bias, no
+  // packed batch with them)
+  const bool store = dropout && p.drop_bits != nullptr;
 #define SDPA_FWD_CASE(DD, CC, RR)                                                    \
   if (D == DD && causal == CC && dropout == RR)                                      \
     return varlen ? launch_fwd_t<DD, CC, RR, true>(maps, p, stream)                  \
                   : (bias ? launch_fwd_bias_t<DD, CC, RR>(maps, p, stream)           \
-                          : launch_fwd_t<DD, CC, RR, false>(maps, p, stream));
+                          : (store && RR ? launch_fwd_t<DD, CC, RR, false, RR>(maps, p, stream) \
+                                         : launch_fwd_t<DD, CC, RR, false>(maps, p, stream)));
   SDPA_FWD_CASE(64, false, false)
   SDPA_FWD_CASE(64, false, true)
   SDPA_FWD_CASE(64, true, false)

@@ -313,3 +313,50 @@ def test_varlen_argument_errors(lib):
     # workspace as for a [batch, H, max_q] problem
     assert (lib.sdpa_bwd_varlen_workspace_size(r(vl), H, D, None)
             == lib.sdpa_bwd_workspace_size(3, H, 128, 256, D))
+
+
+def test_dropout_bits_size(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    # one bit per score of the 128-padded [Sq, Sk] block of every (batch, head)
+    assert sdpa.sdpa_dropout_bits_size(2, 3, 200, 300) == 2 * 3 * 256 * 384 // 8
+    assert sdpa.sdpa_dropout_bits_size(8, 16, 4096, 4096) == 8 * 16 * 4096 * 4096 // 8
+    assert sdpa.sdpa_dropout_bits_size(1, 1, 1, 1) == 128 * 128 // 8
+    assert sdpa.sdpa_dropout_bits_size(0, 3, 200, 300) == 0
+    assert sdpa.sdpa_dropout_bits_size(2, 3, -1, 300) == 0
+    assert sdpa.sdpa_dropout_bits_size(2**30, 2**30, 2**20, 2**20) == 2**64 - 1
+
+
+def test_dropout_bits_argument_errors(lib):
+    import scaled_dot_product_07_gb300 as sdpa
+    B, H, S, D = 2, 4, 300, 64
+    t = desc(B, H, S, D)
+    r = ctypes.byref
+    need = sdpa.sdpa_dropout_bits_size(B, H, S, S)
+
+    def fwd(o, tt=t, p=0.1):
+        return lib.sdpa_fwd_ex(r(tt), r(tt), r(tt), p, 1, 0.125, 1, 0, r(tt),
+                               ctypes.c_void_p(FAKE), r(o), None)
+
+    assert fwd(options(dropout_bits=FAKE + 2, dropout_bits_bytes=need)) == 3  # not 4-byte aligned
+    assert fwd(options(dropout_bits=FAKE, dropout_bits_bytes=need - 4)) == 1  # short
+    # head dims above 128 and an attention bias have no stored-bits path
+    wide = desc(B, H, S, 192)
+    assert fwd(options(dropout_bits=FAKE, dropout_bits_bytes=need), tt=wide) == 2
+    keep = desc(B, H, S, S, stride=(H * S * 304, S * 304, 304, 1))
+    o = options(dropout_bits=FAKE, dropout_bits_bytes=need, attn_bias=ctypes.addressof(keep))
+    assert fwd(o) == 2
+
+    def bwd(o, p=0.1):
+        return lib.sdpa_bwd_ex(r(t), r(t), r(t), r(t), r(t), ctypes.c_void_p(FAKE), p, 1, 0, 0,
+                               0.125, r(t), r(t), r(t), ctypes.c_void_p(FAKE), 1 << 40, r(o), None)
+
+    assert bwd(options(dropout_bits=FAKE, dropout_bits_bytes=need - 1)) == 1
+    assert bwd(options(dropout_bits=FAKE + 1, dropout_bits_bytes=need)) == 3
+    # a packed batch has no stored-bits path
+    vl = sdpa.SdpaVarlen()
+    vl.cu_seqlens_q, vl.cu_seqlens_k, vl.batch, vl.max_seqlen_q, vl.max_seqlen_k = FAKE, FAKE, 2, 128, 128
+    q = desc(1, H, 200, D, layout="BSHE")
+    st = lib.sdpa_fwd_varlen(r(q), r(q), r(q), r(vl), 0.1, 1, 0.125, 0, 0, r(q),
+                             ctypes.c_void_p(FAKE),
+                             r(options(dropout_bits=FAKE, dropout_bits_bytes=1 << 30)), None)
+    assert st == 2
