@@ -85,11 +85,14 @@ def bwd_small_kernel_bytes(w):
 # parameters; the backward forms it at run time (two additions per round)
 # and assembles the quad's keep nibbles (about eight more operations).
 PHILOX_OPS = {"fwd": {"mul_wide": 20, "alu": 28}, "bwd": {"mul_wide": 20, "alu": 56}}
-# Per-SM integer rates used for the bound: the ALU pipe and the FMA pipe
-# (which executes the wide multiplies) each retire 64 lane-operations per
-# clock (16 lanes on each of the four schedulers); the two pipes run in
-# parallel, so the bound is the busier one.
-INT_LANE_OPS_PER_CLK_PER_SM = 64
+# Per-SM rates of the two pipes, in lane-operations per clock: the ALU pipe
+# retires 64 (16 lanes on each of the four schedulers); a 32x32->64-bit
+# multiply takes two issue slots of the 16-lane FMA-heavy pipe, so 32. (The
+# profiled dropout forward's FMA-heavy active cycles match four cycles per
+# warp-wide multiply, and a loop of Philox draws alone saturates at about
+# three quarters of this bound.) The two pipes run in parallel, so the
+# bound is the busier one.
+PIPE_LANE_OPS_PER_CLK_PER_SM = {"mul_wide": 32, "alu": 64}
 SM_COUNT = 152
 
 
@@ -98,21 +101,21 @@ def philox_alu_bound(w, direction, clock_mhz, pass_ms, base_ms, peak_tflops):
     work (the pass's algorithmic flops at the dense bf16 peak) and the integer
     work of its dropout draws -- one Philox group per four visible (query,
     key) pairs (keys past the causal diagonal are not drawn), timed on the
-    busier of the ALU and FMA pipes at the sampled clock. The two run on
+    busier of the ALU and FMA-heavy pipes at the sampled clock. The two run on
     different units and overlap, so the pass can be no faster than the larger
     bound; frac = that bound / the measured pass. dropout_extra_ms, the pass
     less the same pass at p = 0, is the time the draws did not hide."""
     groups = pairs(w) * w.B * w.H / 4
     ops = PHILOX_OPS[direction]
     clk = (clock_mhz or 2070.0) * 1e6
-    per_pipe = {k: groups * n / (INT_LANE_OPS_PER_CLK_PER_SM * SM_COUNT * clk) * 1e3
+    per_pipe = {k: groups * n / (PIPE_LANE_OPS_PER_CLK_PER_SM[k] * SM_COUNT * clk) * 1e3
                 for k, n in ops.items()}
     alu_ms = max(per_pipe.values())
     f_fwd, f_bwd = flops(w)
     tensor_ms = (f_fwd if direction == "fwd" else f_bwd) / (peak_tflops * 1e12) * 1e3
     bound = max(alu_ms, tensor_ms)
     return {"bound": "alu" if alu_ms >= tensor_ms else "tensor", "groups": groups,
-            "ops_per_group": ops, "lane_ops_per_clk_per_sm": INT_LANE_OPS_PER_CLK_PER_SM,
+            "ops_per_group": ops, "lane_ops_per_clk_per_sm": PIPE_LANE_OPS_PER_CLK_PER_SM,
             "sm_count": SM_COUNT, "clock_mhz": clock_mhz, "pipe_ms": per_pipe,
             "alu_bound_ms": alu_ms, "tensor_bound_ms": tensor_ms, "pass_ms": pass_ms,
             "frac": bound / pass_ms if pass_ms > 0 else None,
@@ -736,6 +739,17 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
                                                         peak)
     extras["dropout_0.1"]["alu_bwd"] = philox_alu_bound(wd, "bwd", clock_mhz, bwd_d, base_bwd_ms,
                                                         peak)
+    # the same with the keep bits carried from the forward to the backward
+    bits = torch.empty(sdpa.sdpa_dropout_bits_size(w.B, w.H, w.Sq, w.Sk) // 4, dtype=torch.int32,
+                       device=dev)
+    fwd_s = timed(lambda: sdpa.sdpa_fwd_ex(q, k, v, p_d, w.is_causal, None, w.seed, w.offset,
+                                           out=out, lse=lse, dropout_bits=bits), 5)
+    bwd_s = timed(lambda: sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, p_d, w.is_causal, w.seed,
+                                           w.offset, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                           dropout_bits=bits), 5)
+    extras["dropout_0.1"]["stored_bits"] = stored_bits_line(wd, fwd_s, bwd_s, fwd_d, bwd_d,
+                                                            bits.numel() * 4, peak)
+    del bits
 
     # other head dims on the same B, H, S: 96 (the 128-wide kernels with the
     # last 32 columns zero-filled by TMA) and 256 (the 256-wide kernels)
@@ -804,7 +818,7 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
     # get a 256 MB flush before every call, outside the events)
     for name in ("pages_test", "encoder_dropout", "cross_attn"):
         wl = W.WORKLOADS[name]
-        extras[name] = measure_workload(torch, sdpa, wl, dev, peak)
+        extras[name] = measure_workload(torch, sdpa, wl, dev, peak, stored_bits=True)
         if wl.dropout_p > 0:
             # the same pass without dropout: the dropout's own time
             base = measure_workload(torch, sdpa, W.make_workload(name, dropout_p=0.0), dev, peak)
@@ -819,9 +833,23 @@ def measure_extras(torch, sdpa, W, w, dev, stream, q, k, v, do, out, lse, dq, dk
     return extras
 
 
-def measure_workload(torch, sdpa, w, dev, peak, reps=10):
+def stored_bits_line(w, fwd_ms, bwd_ms, fwd_redraw_ms, bwd_redraw_ms, nbytes, peak):
+    """A dropout pass pair with the keep bits carried from the forward to the
+    backward (dropout_bits): the forward also stores its bits, the backward
+    reads them instead of drawing, so its roofline is its tensor work alone."""
+    f, b = flops(w)
+    return {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "step_ms": fwd_ms + bwd_ms,
+            "step_ms_redrawn": fwd_redraw_ms + bwd_redraw_ms, "bits_bytes": nbytes,
+            "bwd_tflops": b / (bwd_ms * 1e-3) / 1e12,
+            "bwd_frac": b / (bwd_ms * 1e-3) / 1e12 / peak,
+            "note": "forward stores the keep bits, backward reads them (same mask, same "
+                    "results); step_ms_redrawn is the pair that draws them twice"}
+
+
+def measure_workload(torch, sdpa, w, dev, peak, reps=10, stored_bits=False):
     """Forward and backward of one named workload (BHSE), each call timed by
-    its own CUDA events, mean over `reps` calls."""
+    its own CUDA events, mean over `reps` calls; with stored_bits (dropout, D
+    up to 128) also the pair that carries the keep bits in a buffer."""
     q, k, v, do = (x.to(dev) for x in cached_inputs(w))
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
@@ -830,32 +858,46 @@ def measure_workload(torch, sdpa, w, dev, peak, reps=10):
                      device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(64 << 20, dtype=torch.float32, device=dev) if small_l2(w) else None
-    fwd = lambda: sdpa.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset,
-                                out=out, lse=lse)
-    bwd = lambda: sdpa.sdpa_bwd(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed,
-                                w.offset, None, dq=dq, dk=dk, dv=dv, workspace=ws)
-    for _ in range(3):
-        fwd()
-        bwd()
-    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(reps)]
-    torch.cuda.synchronize()
-    for i in range(reps):
-        if flush is not None:
-            flush.fill_(float(i))
-        ev[i][0].record(stream)
-        fwd()
-        ev[i][1].record(stream)
-        if flush is not None:
-            flush.fill_(float(i) + 0.5)
-        ev[i][2].record(stream)
-        bwd()
-        ev[i][3].record(stream)
-    torch.cuda.synchronize()
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+    def time_pair(fwd, bwd):
+        for _ in range(3):
+            fwd()
+            bwd()
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            if flush is not None:
+                flush.fill_(float(i))
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            if flush is not None:
+                flush.fill_(float(i) + 0.5)
+            ev[i][2].record(stream)
+            bwd()
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        return (statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+                statistics.mean(e[2].elapsed_time(e[3]) for e in ev))
+
+    fwd_ms, bwd_ms = time_pair(
+        lambda: sdpa.sdpa_fwd(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset,
+                              out=out, lse=lse),
+        lambda: sdpa.sdpa_bwd(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset,
+                              None, dq=dq, dk=dk, dv=dv, workspace=ws))
     flushed = flush is not None
-    return _pass_line(w, fwd_ms, bwd_ms, workload_config(w)["workload"] +
+    line = _pass_line(w, fwd_ms, bwd_ms, workload_config(w)["workload"] +
                       ("; L2 flushed before each call" if flushed else ""), peak)
+    if stored_bits and w.dropout_p > 0 and w.D <= 128:
+        bits = torch.empty(sdpa.sdpa_dropout_bits_size(w.B, w.H, w.Sq, w.Sk) // 4,
+                           dtype=torch.int32, device=dev)
+        fs, bs = time_pair(
+            lambda: sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset,
+                                     out=out, lse=lse, dropout_bits=bits),
+            lambda: sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed,
+                                     w.offset, dq=dq, dk=dk, dv=dv, workspace=ws,
+                                     dropout_bits=bits))
+        line["stored_bits"] = stored_bits_line(w, fs, bs, fwd_ms, bwd_ms, bits.numel() * 4, peak)
+    return line
 
 
 def measure_e2e(torch, sdpa, w, dev, stream, inputs_cpu, q, k, v, lse, ws, world):

@@ -19,7 +19,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // (which role, which barrier).
 enum WaitSite : uint32_t {
   kSiteFwdKvEmpty = 0x101, kSiteFwdQFull, kSiteFwdKvFull, kSiteFwdSEmpty, kSiteFwdPFull,
-  kSiteFwdSFull, kSiteFwdODone,
+  kSiteFwdSFull, kSiteFwdODone, kSiteFwdBiasFull, kSiteFwdBiasEmpty,
   kSiteBwdKvFull = 0x201, kSiteBwdQFull, kSiteBwdQEmpty, kSiteBwdSpEmpty, kSiteBwdPFull,
   kSiteBwdDsFull, kSiteBwdDqEmpty, kSiteBwdSFull, kSiteBwdDpFull, kSiteBwdPdsEmpty,
   kSiteBwdDqFull, kSiteBwdDone,

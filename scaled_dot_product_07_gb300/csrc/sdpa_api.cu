@@ -190,14 +190,18 @@ bool make_dq_map(CUtensorMap* m, float* acc, int64_t rows) {
   return r == CUDA_SUCCESS;
 }
 
-// Tensor map of an attention bias [Bb, Hb, Sq, Sk] (keys contiguous) for the
-// backward's bias tiles: box [64 query rows x 128 keys], no swizzle, zeros
-// past the edges. A shared (size-1) dim is always read at coordinate 0, so
-// it gets a packed stride.
+// Tensor map of an attention bias (or its gradient) [Bb, Hb, Sq, Sk] (keys
+// contiguous), zeros past the edges: the backward's box is [64 query rows x
+// 128 keys] unswizzled (fwd = false), the forward's [128 query rows x 64
+// keys] with the 128-byte swizzle (fwd = true). A shared dim (size 1 or
+// stride 0) is always read at coordinate 0, so it gets a packed stride.
 bool make_bias_map(CUtensorMap* m, const AttnBias& bias, int64_t Bb, int64_t Hb, int64_t Sq,
-                   int64_t Sk) {
+                   int64_t Sk, bool fwd = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  // a shared dim (size 1 or stride 0) is one slice, read at coordinate 0
+  if (bias.sB == 0) Bb = 1;
+  if (bias.sH == 0) Hb = 1;
   const int64_t rowS = Sq == 1 ? (Sk + 7) / 8 * 8 : bias.sS;
   const int64_t headS = Hb == 1 ? rowS * Sq : bias.sH;
   const int64_t batchS = Bb == 1 ? headS * Hb : bias.sB;
@@ -205,10 +209,11 @@ bool make_bias_map(CUtensorMap* m, const AttnBias& bias, int64_t Bb, int64_t Hb,
                         static_cast<cuuint64_t>(Hb), static_cast<cuuint64_t>(Bb)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(rowS * 2), static_cast<cuuint64_t>(headS * 2),
                            static_cast<cuuint64_t>(batchS * 2)};
-  cuuint32_t box[4] = {128, 64, 1, 1};
+  cuuint32_t box[4] = {fwd ? 64u : 128u, fwd ? 128u : 64u, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(bias.data), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fwd ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -406,9 +411,14 @@ sdpa_status fwd_launch(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_te
   const int64_t Dk = kernel_head_dim(D);
   // the 256-wide forward streams 64-key K / V tiles
   const uint32_t kv_rows = Dk == 256 ? 64 : 128;
-  CUtensorMap maps[4];
+  // q, k, v, out, bias (a copy of q's when there is none)
+  CUtensorMap maps[5];
   if (!make_map(&maps[0], q, 128) || !make_map(&maps[1], k, kv_rows) ||
       !make_map(&maps[2], v, kv_rows) || !make_map(&maps[3], out, 128))
+    return SDPA_ERR_CUDA;
+  maps[4] = maps[0];
+  if (opt.bias.data != nullptr &&
+      !make_bias_map(&maps[4], opt.bias, opt.bias_B, opt.bias_H, Sq, Sk, true))
     return SDPA_ERR_CUDA;
   FwdParams p;
   p.B = static_cast<int>(B);

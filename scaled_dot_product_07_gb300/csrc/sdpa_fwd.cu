@@ -43,9 +43,15 @@
 // Small grids (at most two items per SM) run one item per CTA.
 //
 // With an additive bias the forward is fwd_kernel_bias: the same roles and
-// products, one item per CTA, each softmax thread's 64 bias values fetched
-// with 16-byte loads before its scores are ready, out staged in the dead Q
-// tiles and stored by TMA.
+// products, one item per CTA, plus a warp that loads each score tile's bias
+// tile by TMA into a staging tile the softmax reads before its scores are
+// ready; out staged in the dead Q tiles and stored by TMA.
+//
+// With dropout and a caller's keep-bit buffer (FwdParams::drop_bits), the
+// STORE instantiation also writes each half row's 64 keep bits there for the
+// backward; it draws them before exponentiating and applies them from the
+// bits (its own instantiation, so that the plain dropout kernel's register
+// allocation is untouched).
 #include <type_traits>
 
 #include "common.cuh"
@@ -79,19 +85,26 @@ struct FwdLayout {
 };
 
 // The forward with a bias keeps the same Q, K and V tiles and adds a 32 KB
-// staging area: each softmax thread's 64 bias values of its next tile (128
-// bytes), copied asynchronously while it works on the current one. To make
-// room, the row-max exchange between the two halves of a row uses one slot
-// per (half, row) instead of four.
+// staging tile for the bias of the next score tile: [half 2][row 128][128
+// bytes], each half a 128-byte-swizzled TMA box of 64 keys, so that thread
+// (half, row) finds its 64 values at row*128 + (chunk ^ (row & 7))*16 of its
+// half and a warp's reads of one chunk hit distinct banks. To make room, the
+// row-max exchange between the two halves of a row uses one slot per (half,
+// row) instead of four.
 template <int D>
 struct FwdBiasLayout : FwdLayout<D> {
   using Base = FwdLayout<D>;
   static constexpr int kRed = Base::kRed;                 // [half 2][row 128] fp32
   static constexpr int kBar = kRed + 2 * 128 * 4;
-  static constexpr int kMisc = kBar + Base::kNumBars * 8;
-  static constexpr int kBiasStage = (kMisc + 16 + 127) / 128 * 128;  // [thread 256][128 bytes]
+  // the base set, then bias_full (the TMA has landed the staged tile) and
+  // bias_empty (every softmax thread has read it)
+  static constexpr int kNumBars = Base::kNumBars + 2;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBiasStage = (kMisc + 16 + 1023) / 1024 * 1024;
   static constexpr int kBytes = kBiasStage + 256 * 128;
   static constexpr int kAlloc = kBytes + 1024;
+  // softmax warps 0-7, MMA warp 8, TMA warp 9, bias TMA warp 10
+  static constexpr int kThreads = 352;
   static_assert(kAlloc <= 232448, "shared memory budget");
 };
 
@@ -440,16 +453,22 @@ __global__ void __launch_bounds__(320, 1)
             const float alpha = ex2_approx((m[i] - m_new) * sl2);
             l[i] *= alpha;
             m[i] = m_new;
-            // (not unrolled: the branch is rare, and two chunks of O live
-            // beside the scores made the kernel spill registers)
-  #pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {  // this half's D/2 columns of O
+            auto rescale = [&](int c) {  // 32 of this half's D/2 columns of O
               uint32_t o[32];
               tmem_ld32(tO + (D / 2) * half + c * 32, o);
               tmem_ld_wait(o);
   #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
               tmem_st32(tO + (D / 2) * half + c * 32, o);
+            };
+            if constexpr (DROPOUT) {
+              // not unrolled beside the Philox chains' registers (measured
+              // faster there; unrolled is faster without dropout)
+  #pragma unroll 1
+              for (int c = 0; c < D / 64; ++c) rescale(c);
+            } else {
+  #pragma unroll
+              for (int c = 0; c < D / 64; ++c) rescale(c);
             }
           }
           const float neg = -m[i] * sl2;
@@ -591,15 +610,20 @@ __global__ void __launch_bounds__(320, 1)
 
 // The forward with an additive bias: one item (query-tile pair) per CTA, O
 // staged in the dead Q tiles and stored by TMA. The same algorithm as
-// fwd_kernel; kept as its own kernel because with a bias it runs 1.19 ms
+// fwd_kernel; kept as its own kernel because with a bias it ran 1.19 ms
 // against fwd_kernel's 1.38 (B8 H16 S4096 D128 causal, relative-position
-// bias [1,H,S,S]). Packed batches take no bias, so it has no packed form.
+// bias [1,H,S,S]). A warp of its own (warp 10) loads each score tile's bias
+// by TMA into one staging tile, which the softmax reads and releases before
+// its scores are ready: 0.61 ms, against 1.03 with each thread copying its
+// own 128 bytes with cp.async. Packed batches take no bias, so it has no
+// packed form.
 template <int D, bool CAUSAL, bool DROPOUT>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fwd_kernel_bias(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_o,
+                    const __grid_constant__ CUtensorMap tm_bias, const FwdParams p) {
   constexpr bool BIAS = true;
   using L = FwdBiasLayout<D>;
   constexpr int S = L::kStages;
@@ -617,6 +641,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* s_full = v_empty + S;    // [2]
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_full = p_full + 2;     // [2]
+  uint64_t* bias_full = bars + L::Base::kNumBars;
+  uint64_t* bias_empty = bias_full + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   uint32_t* abort_word = reinterpret_cast<uint32_t*>(smem + L::kMisc + 4);
 
@@ -653,6 +679,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&p_full[i], 256);
       mbar_init(&o_full[i], 1);
     }
+    mbar_init(bias_full, 1);
+    mbar_init(bias_empty, 256);
     *abort_word = 0u;
     fence_mbar_init();
   }
@@ -666,7 +694,32 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_holder;
   const WaitCtl wc{abort_word, p.err, p.wait_limit_ns};
 
-  if (warp == 9) {
+  if (warp == 10) {
+    // ------------------------------------------------------------ bias TMA
+    // The bias tile of every score tile, in the order the softmax visits
+    // them, into the one staging tile once the softmax has read the previous
+    // one. Keys past Sk and rows past Sq read as zeros.
+    if (lane == 0) {
+      prefetch_tmap(&tm_bias);
+      const int hb = p.bias.sH != 0 ? h : 0;
+      const int bb = p.bias.sB != 0 ? b : 0;
+      int t = 0;  // tiles loaded
+      for (int j = 0; j < n_kv; ++j) {
+        for (int i = 0; i < 2; ++i) {
+          if (j >= n_t[i]) continue;
+          if (t >= 1) mbar_wait(bias_empty, (t - 1) & 1, wc, kSiteFwdBiasEmpty);
+          ++t;
+          mbar_arrive_expect_tx(bias_full, 256 * 128);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            tma_load_4d(smem + L::kBiasStage + hf * 128 * 128, &tm_bias, bias_full,
+                        j * 128 + 64 * hf, q0 + 128 * i, hb, bb);
+        }
+      }
+      if (*abort_word && t >= 1) mbar_wait_drain(bias_full, (t - 1) & 1, 2000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -796,40 +849,10 @@ __global__ void __launch_bounds__(320, 1)
       (void)j;
       return fmaxf(mh, exchange(i, mh));
     };
-    // The bias values of tile (i, j) for this thread -- keys [j*128 + 64 half,
-    // +64) of row q0 + 128 i + row -- copied asynchronously into its own 128
-    // bytes of the staging area (16-byte chunks placed so that a warp's
-    // reads of one chunk hit distinct banks). Keys past Sk read as zeros.
+    // this thread's 64 bias values of the staged tile -- keys [j*128 + 64
+    // half, +64) of row q0 + 128 i + row -- in its half's swizzled box
     const uint32_t bstage = sb + L::kBiasStage + (half * 128 + row) * 128;
-    auto fetch_bias = [&](int i, int j) {
-      const int kb = j * 128 + 64 * half;
-      const uint16_t* rp = p.bias.data + b * p.bias.sB + h * p.bias.sH +
-                           static_cast<int64_t>(min(q0 + 128 * i + row, Sq - 1)) * p.bias.sS;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int nv = min(max(Sk - (kb + 8 * c), 0), 8);
-        cp_async16(bstage + ((c ^ (row & 7)) << 4), nv > 0 ? rp + kb + 8 * c : rp, 2 * nv);
-      }
-      cp_async_commit();
-    };
-    // the tile after (i, j) in the order the loop visits them
-    auto next_tile = [&](int i, int j, int& i2, int& j2) {
-      for (;;) {
-        if (i == 0) {
-          i = 1;
-        } else {
-          i = 0;
-          ++j;
-        }
-        if (j >= n_kv) return false;
-        if (j < n_t[i]) {
-          i2 = i;
-          j2 = j;
-          return true;
-        }
-      }
-    };
-    if (n_kv > 0) fetch_bias(n_t[0] > 0 ? 0 : 1, 0);
+    int bias_read = 0;  // bias tiles read
 
     for (int j = 0; j < n_kv; ++j) {
       for (int i = 0; i < 2; ++i) {
@@ -837,12 +860,14 @@ __global__ void __launch_bounds__(320, 1)
         const int qi = q0 + 128 * i + row;
         const uint32_t tS = tmem + L::tmem_s(i) + lane_base;
         const uint32_t tO = tmem + L::tmem_o(i) + lane_base;
-        // the half row's 64 bias values: this tile's copy (issued one tile
-        // ahead) has landed
+        // the staged bias tile, read and released before the scores are
+        // ready, so that the next one loads while this tile is worked on
         uint4 bv[8];
-        cp_async_wait_all();
+        mbar_wait(bias_full, bias_read & 1, wc, kSiteFwdBiasFull);
+        ++bias_read;
 #pragma unroll
         for (int c = 0; c < 8; ++c) bv[c] = ld_shared_v4(bstage + ((c ^ (row & 7)) << 4));
+        mbar_arrive(bias_empty);
         mbar_wait(&s_full[i], j & 1, wc, kSiteFwdSFull);
         tc_fence_after();
         uint32_t r0[32], r1[32];
@@ -868,9 +893,6 @@ __global__ void __launch_bounds__(320, 1)
               x[8 * c + 2 * e + 1] = fmaf(bf16_bits_to_float(w[e] >> 16), inv, x[8 * c + 2 * e + 1]);
             }
           }
-          // the staging slot is free again: start the next tile's copy
-          int i2 = 0, j2 = 0;
-          if (next_tile(i, j, i2, j2)) fetch_bias(i2, j2);
         }
         const int k0 = j * 128 + 64 * half;  // first key of this half
         if ((k0 + 64 > Sk) || (CAUSAL && k0 + 63 > q0 + 128 * i)) {
@@ -1025,7 +1047,8 @@ cudaError_t launch_fwd_bias_t(const CUtensorMap* maps, const FwdParams& p, cudaS
   cudaError_t e = ensure_smem_attr<fwd_kernel_bias<D, C, DR>>(smem);
   if (e != cudaSuccess) return e;
   const unsigned items = static_cast<unsigned>(p.n_q_tiles) * static_cast<unsigned>(p.B * p.H);
-  kern<<<items, FwdLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  kern<<<items, FwdBiasLayout<D>::kThreads, smem, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                            maps[4], p);
   return cudaGetLastError();
 }
 

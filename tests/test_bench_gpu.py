@@ -36,3 +36,4 @@ def test_default_bench_path_prints_a_complete_line(cuda_lib):
         assert name in line["extended"], name
     for name in ("dropout_0.1", "encoder_dropout", "cross_attn"):
         assert line["extended"][name]["alu_fwd"]["alu_bound_ms"] > 0, name
+        assert line["extended"][name]["stored_bits"]["bwd_ms"] > 0, name

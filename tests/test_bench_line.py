@@ -94,16 +94,36 @@ def test_clock_window_keeps_only_its_samples_and_flags_throttling():
 
 
 def test_philox_alu_bound_of_the_decoder_forward():
-    """One Philox group per four visible pairs; the ALU bound is the busier of
-    the ALU and FMA pipes at 64 lane-operations per clock per SM, and the
-    pass's roofline the larger of that and its tensor bound."""
+    """One Philox group per four visible pairs; the integer bound is the
+    busier of the ALU pipe (64 lane-operations per clock per SM) and the
+    FMA-heavy pipe's wide multiplies (32 per clock per SM), and the pass's
+    roofline the larger of that and its tensor bound."""
     w = W.make_workload("decoder_long", dropout_p=0.1)
     groups = 4096 * 4097 // 2 * 8 * 16 / 4
     r = bench.philox_alu_bound(w, "fwd", 2000.0, 1.35, 0.41, 1940.8)
     assert r["groups"] == groups
     alu_ms = groups * bench.PHILOX_OPS["fwd"]["alu"] / (64 * 152 * 2000e6) * 1e3
-    assert abs(r["alu_bound_ms"] - alu_ms) < 1e-12  # 28 ALU ops per group outweigh 20 multiplies
+    mul_ms = groups * bench.PHILOX_OPS["fwd"]["mul_wide"] / (32 * 152 * 2000e6) * 1e3
+    assert mul_ms > alu_ms  # 20 wide multiplies at half rate outweigh 28 ALU operations
+    assert abs(r["alu_bound_ms"] - mul_ms) < 1e-12
+    # the backward forms its round keys and quad nibbles: the ALU pipe is busier
+    rb = bench.philox_alu_bound(w, "bwd", 2000.0, 2.0, 1.36, 1940.8)
+    assert abs(rb["alu_bound_ms"] - groups * 56 / (64 * 152 * 2000e6) * 1e3) < 1e-12
+    alu_ms = mul_ms
     tensor_ms = bench.flops(w)[0] / 1940.8e12 * 1e3
     assert abs(r["tensor_bound_ms"] - tensor_ms) < 1e-12
     assert r["bound"] == "alu" and abs(r["frac"] - max(alu_ms, tensor_ms) / 1.35) < 1e-12
     assert abs(r["dropout_extra_ms"] - 0.94) < 1e-12
+
+
+def test_stored_bits_line():
+    """The dropout pair with the keep bits carried in a buffer: its step is
+    the two passes, beside the pair that draws them twice, and its backward
+    is read against the tensor peak alone."""
+    w = W.make_workload("decoder_long", dropout_p=0.1)
+    r = bench.stored_bits_line(w, 1.5, 1.46, 1.31, 2.03, 268435456, 1940.8)
+    assert abs(r["step_ms"] - 2.96) < 1e-12 and abs(r["step_ms_redrawn"] - 3.34) < 1e-12
+    b = bench.flops(w)[1]
+    assert abs(r["bwd_tflops"] - b / 1.46e-3 / 1e12) < 1e-9
+    assert abs(r["bwd_frac"] - r["bwd_tflops"] / 1940.8) < 1e-12
+    assert r["bits_bytes"] == 268435456
