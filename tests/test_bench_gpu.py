@@ -29,6 +29,7 @@ def test_default_bench_path_prints_a_complete_line(cuda_lib):
         assert line[key] is not None, key
     assert line["value"] > 0 and line["roofline"]["achieved"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
+    assert 0 < line["e2e"]["copy_bound"]["frac"] <= 1.5
     assert line["cpu_baseline"]["cores"] >= 1
     assert line["sustained"]["steps"] > 0
     for name in ("graph_step", "bwd_deterministic", "dropout_0.1", "attn_bias", "varlen",
