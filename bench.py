@@ -580,12 +580,15 @@ def bench_ours(args, w):
     # profiling the bias path: a relative-position bias shared by the batch
     bias = (W.padded_rows(W.draw_bias((1, w.H, w.Sq, w.Sk), w.input_seed + 17, "relpos").to(dev))
             if args.bias else None)
+    # profiling the dropout path with the keep bits carried forward to backward
+    bits = (torch.empty(sdpa.sdpa_dropout_bits_size(w.B, w.H, w.Sq, w.Sk) // 4, dtype=torch.int32,
+                        device=dev) if args.stored_bits else None)
 
     def step():
         sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset,
-                         attn_bias=bias, out=out, lse=lse)
+                         attn_bias=bias, out=out, lse=lse, dropout_bits=bits)
         sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
-                         attn_bias=bias, dq=dq, dk=dk, dv=dv, workspace=ws)
+                         attn_bias=bias, dq=dq, dk=dk, dv=dv, workspace=ws, dropout_bits=bits)
 
     warmup = max(args.warmup, 3)
     for _ in range(warmup):
@@ -620,11 +623,11 @@ def bench_ours(args, w):
             flush.fill_(float(i))
         ev[i][0].record(stream)
         sdpa.sdpa_fwd_ex(q, k, v, w.dropout_p, w.is_causal, None, w.seed, w.offset, out=out,
-                         lse=lse, attn_bias=bias, kernel_events=km[i][0:2])
+                         lse=lse, attn_bias=bias, kernel_events=km[i][0:2], dropout_bits=bits)
         ev[i][1].record(stream)
         sdpa.sdpa_bwd_ex(do, q, k, v, out, lse, w.dropout_p, w.is_causal, w.seed, w.offset, None,
                          attn_bias=bias, dq=dq, dk=dk, dv=dv, workspace=ws,
-                         kernel_events=km[i][2:4])
+                         kernel_events=km[i][2:4], dropout_bits=bits)
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -678,6 +681,8 @@ def bench_ours(args, w):
                          extras, e2e, cpu)
     if bias is not None:
         line["config"]["bias"] = "relative-position [1, H, Sq, Sk] bf16 (profiling case)"
+    if bits is not None:
+        line["config"]["stored_bits"] = "keep bits carried forward to backward (profiling case)"
     print(json.dumps(line))
     return 0
 
@@ -1028,6 +1033,9 @@ def main(argv=None):
     ap.add_argument("--bias", choices=["relpos"], default=None,
                     help="add a relative-position bias [1, H, Sq, Sk] to every call (profiling "
                          "the bias path; not a bench line)")
+    ap.add_argument("--stored-bits", action="store_true",
+                    help="carry the dropout keep bits from forward to backward in a buffer "
+                         "(profiling that path; not a bench line)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another named workload of the package's workloads module (its own "
                          "shape; the bench line is the default one)")
