@@ -13,7 +13,10 @@
 //               thread = key row. P^T = exp2(S^T*scale*log2e - lse2) (masked,
 //               dropout applied) is stored as bf16 into TMEM (A operand of
 //               dV += P~^T dO); dS^T = P^T (dP~^T keep/(1-p) - Delta) is
-//               stored as bf16 into shared memory (operand of dK and dQ).
+//               stored as bf16 into shared memory (B operand of dQ^T) and
+//               into the step's S^T columns [32, 64) of TMEM (A operand of
+//               dK += dS^T Q, which so reads only Q from shared memory: the
+//               kernel is bound by shared-memory bandwidth).
 //   warps 8-11  dQ warpgroup: reads the dQ^T partial of a step from TMEM,
 //               stages it fp32 [64 x 128] and reduces it into the global fp32
 //               accumulator with four bulk reduce-adds (one per warp).
@@ -245,7 +248,6 @@ __global__ void __launch_bounds__(448, 1)
         const int st = u % NS;
         const uint64_t d_qmn = sdesc_sw128(sb + L::kQ + st * L::kQBytes, L::kQSlab, 1024);
         const uint64_t d_omn = sdesc_sw128(sb + L::kDO + st * L::kQBytes, L::kQSlab, 1024);
-        const uint64_t d_ds = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, 16, 1024);
         const uint64_t d_dsmn = sdesc_sw128(sb + L::kDs + x * L::kDsBytes, L::kDsBytes, 1024);
         mbar_wait_t<kInlineWaits>(&p_full[x], (u >> 1) & 1, wc, kSiteBwdPFull);
         tc_fence_after();
@@ -256,10 +258,11 @@ __global__ void __launch_bounds__(448, 1)
                          sdesc_add(d_omn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
         mbar_wait_t<kInlineWaits>(&ds_full[x], (u >> 1) & 1, wc, kSiteBwdDsFull);
         tc_fence_after();
-        // dK += dS^T Q: A = dS^T smem K-major, B = Q MN-major
+        // dK += dS^T Q: A = dS^T bf16 in TMEM (S^T columns [32, 64), written by
+        // the compute warpgroup beside its shared-memory copy), B = Q MN-major
 #pragma unroll
         for (int kk = 0; kk < MQ / 16; ++kk)
-          mma_bf16_ss_if(leader, tmem + L::kTmemDK, sdesc_add(d_ds, kk * 32),
+          mma_bf16_ts_if(leader, tmem + L::kTmemDK, tmem + L::tmem_s(x) + 32 + kk * 8,
                          sdesc_add(d_qmn, kk * 2048), kIdKV, (u > 0 || kk > 0) ? 1u : 0u);
         // dQ^T [D x MQ] = K^T dS^T: A = K tile MN-major, B = dS^T MN-major; it
         // overwrites this step's dP^T columns (the compute warpgroup read them
@@ -430,15 +433,23 @@ __global__ void __launch_bounds__(448, 1)
           for (int i = 0; i < 32; ++i)
             st_shared_u16(bias_s + (cc * 32 + i) * 256, pack_bf16x2(ds[i], 0.f) & 0xffffu);
         }
+        // dS^T (bf16 pairs along the query rows) to shared memory, the B
+        // operand of dQ^T, and into S^T columns [32, 64) of TMEM (read
+        // above), the A operand of dK: that product then reads no operand of
+        // this step's from shared memory but Q
+        uint32_t dsw[16];
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const int c = cc * 4 + q4;  // 16-byte chunk along the 128-byte row
-          st_shared_v4(da + sw128_offset(r, c), pack_bf16x2(ds[8 * q4 + 0], ds[8 * q4 + 1]),
-                       pack_bf16x2(ds[8 * q4 + 2], ds[8 * q4 + 3]),
-                       pack_bf16x2(ds[8 * q4 + 4], ds[8 * q4 + 5]),
-                       pack_bf16x2(ds[8 * q4 + 6], ds[8 * q4 + 7]));
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dsw[4 * q4 + e] = pack_bf16x2(ds[8 * q4 + 2 * e], ds[8 * q4 + 2 * e + 1]);
+          st_shared_v4(da + sw128_offset(r, c), dsw[4 * q4], dsw[4 * q4 + 1], dsw[4 * q4 + 2],
+                       dsw[4 * q4 + 3]);
         }
+        tmem_st16(tS + 32 + 16 * cc, dsw);
       }
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sp_empty[x]);
       fence_async_smem();
