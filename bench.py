@@ -1001,17 +1001,25 @@ def measure_e2e(torch, sdpa, w, dev, stream, inputs_cpu, q, k, v, lse, ws, world
     for t in range(NB):
         copies_only(t)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for t in range(e2e_steps):
-        copies_only(t)
-    torch.cuda.synchronize()
-    copy_ms = barrier_max((time.perf_counter() - t0) * 1e3, world) / e2e_steps
+    # the fastest of three loops: inside this process the copies-alone loop
+    # now and then ran far slower than the same copies in a fresh process
+    # (3.2 ms per step there), while the pipelined step above did not
+    runs = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        for t in range(e2e_steps // 3):
+            copies_only(t)
+        torch.cuda.synchronize()
+        runs.append((time.perf_counter() - t0) * 1e3 / (e2e_steps // 3))
+    copy_ms = barrier_max(min(runs), world)
     return {"value": world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
             "copies_declared": True,
             "copy_bound": {"ms_per_step": copy_ms, "frac": copy_ms / e2e_ms,
+                           "runs_ms": runs,
                            "note": "the step's uploads and downloads alone, concurrently on "
-                                   "two streams (no kernels): the host link's bound"},
+                                   "two streams (no kernels), the fastest of three loops: the "
+                                   "host link's bound"},
             "timing": "host wall clock around 40 pipelined steps, synchronised on both sides"}
 
 
