@@ -95,9 +95,9 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 
 /*
  * sdpa_bwd_workspace_size — bytes of device workspace sdpa_bwd needs for
- * this problem size: an fp32 dQ accumulator of Dk-wide rows (Dk = 128 for
- * D <= 128, whose backward runs on 128-wide tiles, and 256 above) and two
- * fp32 row vectors, with Sq rounded up to a multiple of 128:
+ * this problem size: an fp32 dQ accumulator of Dk-wide rows (Dk = 64 for
+ * D <= 64, 128 for D <= 128, whose backward runs on 128-wide tiles, and 256
+ * above) and two fp32 row vectors, with Sq rounded up to a multiple of 128:
  * B*H*ceil128(Sq)*(Dk + 2)*4 bytes.
  * Returns 0 for an empty problem, and SIZE_MAX when the size does not fit in
  * 62 bits (no workspace then satisfies sdpa_bwd, which returns

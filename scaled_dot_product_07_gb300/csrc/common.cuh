@@ -104,6 +104,7 @@ struct BwdParams {
   int D_io;                 // the caller's head dim (columns of dk, dv)
   StridedBf16 dk_io, dv_io; // for the direct stores of a sequence's last key tile
   StridedBf16 k_io;         // k, read row by row by the 256-wide kernel (K into TMEM)
+  int acc_w;              // dQ accumulator row width: 64 when D <= 64, else 128
   float* dq_acc;          // workspace [B*H, Sq_pad, D] fp32 (reduce-add), or
   float* dq_part;         // deterministic mode: [n_kv_tiles][B*H, Sq_pad, D] fp32,
   size_t part_stride;     // one plain-stored partial per key tile (floats per slice)
@@ -151,12 +152,15 @@ struct SumParams {
 };
 
 // Float offset of element (row i, column c) of (batch, head) bh in the fp32
-// dQ accumulator (or one deterministic-mode slice) of a backward of kernel
-// head dim D: the columns are split into blocks of 128, and each block's
-// rows are contiguous, [B*H][D/128][Sq_pad][128] (at D = 128 plain rows).
+// dQ accumulator (or one deterministic-mode slice) of width D (64 for head
+// dims up to 64, else the backward kernel's 128 or 256): the columns are
+// split into blocks of w = min(D, 128) = 2^sh, and each block's rows are
+// contiguous, [B*H][D/w][Sq_pad][w] (plain rows at D = 64 and 128).
 __host__ __device__ __forceinline__ size_t dq_acc_offset(int64_t bh, int64_t i, int c, int D,
                                                         int Sq_pad) {
-  return ((static_cast<size_t>(bh) * (D >> 7) + (c >> 7)) * Sq_pad + i) * 128 + (c & 127);
+  const int sh = D == 64 ? 6 : 7;
+  return (((static_cast<size_t>(bh) * (D >> sh) + (c >> sh)) * Sq_pad + i) << sh) +
+         (c & ((1 << sh) - 1));
 }
 
 // Opt the kernel into `bytes` of dynamic shared memory, once per device: later

@@ -177,11 +177,11 @@ bool make_map(CUtensorMap* m, const sdpa_tensor* t, uint32_t box_rows) {
 // Tensor map of the fp32 dQ accumulator as a [rows, 128] matrix (rows =
 // B*H*Sq_pad): box [64 rows x 32 columns], the columns one dQ warp of the
 // backward holds for a 64-row query step; no swizzle.
-bool make_dq_map(CUtensorMap* m, float* acc, int64_t rows) {
+bool make_dq_map(CUtensorMap* m, float* acc, int64_t rows, int64_t width) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {128 * 4};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(width * 4)};
   cuuint32_t box[2] = {32, 64};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, acc, dims, strides, box, estr,
@@ -260,6 +260,12 @@ int64_t kernel_head_dim(int64_t D) { return D <= 64 ? 64 : (D <= 128 ? 128 : 256
 // run the 256-wide kernel. The fp32 dQ rows of the workspace are as wide as
 // the kernel's head dim.
 int64_t bwd_kernel_head_dim(int64_t D) { return D <= 128 ? 128 : 256; }
+
+// Columns of the backward's fp32 dQ accumulator: the kernel's width, except
+// that head dims up to 64 (run on the 128-wide kernel, whose dQ columns past
+// 64 are zeros) keep only 64, which halves the bytes its zero-fill, its
+// reduce-adds and its conversion move.
+int64_t dq_acc_width(int64_t D) { return D <= 64 ? 64 : bwd_kernel_head_dim(D); }
 
 // Resolved sdpa_options.
 struct Opts {
@@ -486,7 +492,8 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   // workspace: [dQ accumulator | per-key-tile dQ partials (deterministic)], lse2, delta
   const int64_t Sq_pad = round_up(Sq, 128);
   const int64_t n_kv = (Sk + 127) / 128;
-  const int64_t slice = B * H * Sq_pad * Dk;
+  const int64_t Da = dq_acc_width(D);
+  const int64_t slice = B * H * Sq_pad * Da;
   float* dq_region = static_cast<float*>(workspace);
   float* lse2 = dq_region + slice * (opt.det ? n_kv : 1);
   float* delta = lse2 + B * H * Sq_pad;
@@ -502,7 +509,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   maps[7] = maps[0];
   maps[8] = maps[0];
   // the packed-batch form of the 128-wide kernel reduces dQ through a 2-D map
-  if (Dk == 128 && dq_acc != nullptr && !make_dq_map(&maps[8], dq_acc, B * H * Sq_pad))
+  if (Dk == 128 && dq_acc != nullptr && !make_dq_map(&maps[8], dq_acc, B * H * Sq_pad, Da))
     return SDPA_ERR_CUDA;
   if (opt.bias.data != nullptr &&
       !make_bias_map(&maps[6], opt.bias, opt.bias_B, opt.bias_H, Sq, Sk))
@@ -520,7 +527,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   pp.H = static_cast<int>(H);
   pp.Sq = static_cast<int>(Sq);
   pp.Sq_pad = static_cast<int>(Sq_pad);
-  pp.D = static_cast<int>(Dk);
+  pp.D = static_cast<int>(Da);
   pp.D_io = static_cast<int>(D);
   pp.out = strided(out);
   pp.dout = strided(dout);
@@ -563,6 +570,7 @@ sdpa_status bwd_launch(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa
   p.dk_io = strided(dk);
   p.dv_io = strided(dv);
   p.k_io = strided(k);
+  p.acc_w = static_cast<int>(Da < 128 ? Da : 128);
   p.dq_acc = dq_acc;
   p.dq_part = opt.det ? dq_region : nullptr;
   p.part_stride = static_cast<size_t>(slice);
@@ -682,7 +690,7 @@ sdpa_status sdpa_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 size_t sdpa_bwd_workspace_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D) {
   (void)Sk;
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0) return 0;
-  return checked_bytes(B, H, round_up(Sq, 128), bwd_kernel_head_dim(D) + 2);
+  return checked_bytes(B, H, round_up(Sq, 128), dq_acc_width(D) + 2);
 }
 
 size_t sdpa_dropout_bits_size(int64_t B, int64_t H, int64_t Sq, int64_t Sk) {
@@ -699,7 +707,7 @@ size_t sdpa_bwd_workspace_size_ex(int64_t B, int64_t H, int64_t Sq, int64_t Sk, 
                                   const sdpa_options* options) {
   if (!options || !options->deterministic) return sdpa_bwd_workspace_size(B, H, Sq, Sk, D);
   if (B <= 0 || H <= 0 || Sq <= 0 || D <= 0 || Sk <= 0) return 0;
-  return checked_bytes(B, H, round_up(Sq, 128), bwd_kernel_head_dim(D) * ((Sk + 127) / 128) + 2);
+  return checked_bytes(B, H, round_up(Sq, 128), dq_acc_width(D) * ((Sk + 127) / 128) + 2);
 }
 
 sdpa_status sdpa_bwd_ex(const sdpa_tensor* dout, const sdpa_tensor* q, const sdpa_tensor* k,

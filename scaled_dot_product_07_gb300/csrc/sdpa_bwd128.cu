@@ -29,6 +29,8 @@
 // MMA order per step t: S^T(t), dP^T(t), then dV, dK, dQ of step t-1, so
 // the tensor core computes the next step's products while a compute
 // warpgroup works on the current one.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sdpa {
@@ -493,39 +495,56 @@ __global__ void __launch_bounds__(448, 1)
         // lengths; 4 % slower than the bulk form on the long decoder).
         const int wq = lt >> 5;
         const uint32_t qw = qa + wq * (L::kDqBytes / 4);
-        if (lane == 0) bulk_wait_read_all();  // this warp's previous reduce has read its quarter
-        __syncwarp();
+        // (a 64-wide accumulator, head dims up to 64, has no columns for
+        // warps 2 and 3: theirs are zeros)
+        if (32 * wq < p.acc_w) {
+          if (lane == 0) bulk_wait_read_all();  // this warp's previous reduce has read its quarter
+          __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          st_shared_f32(qw + (c * 32 + lane) * 4, __uint_as_float(r0[c]));
-          st_shared_f32(qw + ((32 + c) * 32 + lane) * 4, __uint_as_float(r1[c]));
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_2d(&tm_dq, smem + L::kDq + wq * (L::kDqBytes / 4), 32 * wq,
-                            bh * p.Sq_pad + i0);
-          bulk_commit();
+          for (int c = 0; c < 32; ++c) {
+            st_shared_f32(qw + (c * 32 + lane) * 4, __uint_as_float(r0[c]));
+            st_shared_f32(qw + ((32 + c) * 32 + lane) * 4, __uint_as_float(r1[c]));
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_dq, smem + L::kDq + wq * (L::kDqBytes / 4), 32 * wq,
+                              bh * p.Sq_pad + i0);
+            bulk_commit();
+          }
         }
       } else {
-        // the whole tile, row-major [MQ][D] fp32; each warp's first lane
-        // reduces (deterministic mode: stores into this key tile's slice) a
-        // quarter of it, 16 rows, so four bulk operations are in flight
-        if ((lt & 31) == 0) bulk_wait_read_all();  // the previous copies have read the tile
-        named_barrier_sync(2, 128);
+        // the whole tile, row-major [MQ][aw] fp32 with aw = 128, or 64 for
+        // head dims up to 64, whose columns past 64 are zeros and are
+        // neither staged nor reduced (aw a compile-time constant in each
+        // branch: a runtime row width cost the 128-wide case 10 %); each
+        // warp's first lane reduces (deterministic mode: stores into this
+        // key tile's slice) a quarter of it, 16 rows, so four bulk
+        // operations are in flight
+        auto stage = [&](auto width) {
+          constexpr int aw = decltype(width)::value;
+          if ((lt & 31) == 0) bulk_wait_read_all();  // the previous copies have read the tile
+          named_barrier_sync(2, 128);
+          if (aw == 128 || lt < aw) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          st_shared_f32(qa + (c * 128 + lt) * 4, __uint_as_float(r0[c]));
-          st_shared_f32(qa + ((32 + c) * 128 + lt) * 4, __uint_as_float(r1[c]));
-        }
-        fence_async_smem();
-        named_barrier_sync(2, 128);
-        if ((lt & 31) == 0) {
-          const int hh = lt >> 5;
-          dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0 + 16 * hh) * 128,
-                 smem + L::kDq + hh * (L::kDqBytes / 4), L::kDqBytes / 4);
-          bulk_commit();
-        }
+            for (int c = 0; c < 32; ++c) {
+              st_shared_f32(qa + (c * aw + lt) * 4, __uint_as_float(r0[c]));
+              st_shared_f32(qa + ((32 + c) * aw + lt) * 4, __uint_as_float(r1[c]));
+            }
+          }
+          fence_async_smem();
+          named_barrier_sync(2, 128);
+          if ((lt & 31) == 0) {
+            const int hh = lt >> 5;
+            dq_out(p.dq_acc, part, (static_cast<size_t>(bh) * p.Sq_pad + i0 + 16 * hh) * aw,
+                   smem + L::kDq + hh * 16 * aw * 4, 16 * aw * 4);
+            bulk_commit();
+          }
+        };
+        if (p.acc_w == 64)
+          stage(std::integral_constant<int, 64>{});
+        else
+          stage(std::integral_constant<int, 128>{});
       }
     }
     if ((lt & 31) == 0) bulk_wait_all();

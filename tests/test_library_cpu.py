@@ -55,12 +55,12 @@ def test_status_strings(lib):
 def test_workspace_size(lib):
     import scaled_dot_product_07_gb300 as sdpa
     # fp32 dQ accumulator + two fp32 row vectors, Sq rounded up to 128
-    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (128 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 64) == 2 * 3 * 256 * (64 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(8, 16, 4096, 4096, 128) == 8 * 16 * 4096 * 130 * 4
     assert sdpa.sdpa_bwd_workspace_size(0, 3, 200, 77, 64) == 0
-    # the backward runs every head dim up to 128 on 128-wide tiles: 128-wide
-    # accumulator rows; above 128 on 256-wide tiles
-    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (128 + 2) * 4
+    # head dims up to 64 keep 64-wide accumulator rows, up to 128 128-wide
+    # rows (the 128-wide tiles of the backward), above 128 256-wide rows
+    assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 40) == 2 * 3 * 256 * (64 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 96) == 2 * 3 * 256 * (128 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 136) == 2 * 3 * 256 * (256 + 2) * 4
     assert sdpa.sdpa_bwd_workspace_size(2, 3, 200, 77, 256) == 2 * 3 * 256 * (256 + 2) * 4
@@ -210,7 +210,7 @@ def options(**kw):
 def test_deterministic_workspace_holds_one_dq_slice_per_key_tile(lib):
     import scaled_dot_product_07_gb300 as sdpa
     # one fp32 [B*H, ceil128(Sq), D] slice per 128-key tile, plus lse2 and delta
-    assert sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, True) == 2 * 3 * 256 * (128 * 3 + 2) * 4
+    assert sdpa.sdpa_bwd_workspace_size_ex(2, 3, 200, 300, 64, True) == 2 * 3 * 256 * (64 * 3 + 2) * 4
     assert (sdpa.sdpa_bwd_workspace_size_ex(8, 16, 4096, 4096, 128, True)
             == 8 * 16 * 4096 * (128 * 32 + 2) * 4)
     # without the flag (or with no options at all) it is the plain workspace
