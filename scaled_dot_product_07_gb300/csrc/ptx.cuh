@@ -108,6 +108,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed
+// sleeps until it completes or up to 20 us, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(20000)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared state of the bounded waits of one CTA. A wait that runs past
 // `limit_ns` records `site` in the global error word, raises the CTA's abort
 // flag and returns; every later wait of the CTA returns at once, so all roles
@@ -119,11 +133,14 @@ struct WaitCtl {
   uint64_t limit_ns;
 };
 
+// kSleep: each poll sleeps in try_wait (up to 20 us) instead of returning
+// at once, which takes polls off the shared-memory pipe.
+template <bool kSleep>
 __device__ __forceinline__ void mbar_wait_poll(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
                                                uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return;
+    if (kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return;
     if (*wc.abort_flag) return;
     if ((it & 15u) == 0 && global_timer_ns() - t0 > wc.limit_ns) {
       *wc.abort_flag = 1u;
@@ -136,13 +153,16 @@ __device__ __forceinline__ void mbar_wait_poll(uint64_t* bar, uint32_t parity, c
 
 static __device__ __noinline__ void mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
                                             uint32_t site) {
-  mbar_wait_poll(bar, parity, wc, site);
+  mbar_wait_poll<true>(bar, parity, wc, site);
 }
 
 // The polling loop sits out of line (a call) in mbar_wait, which keeps the
 // code of kernels with many waits small, and inline in mbar_wait_t<true>: a
 // call makes the caller spill the registers it keeps live across it, which
-// costs the kernels whose loops are short of registers.
+// costs the kernels whose loops are short of registers. The out-of-line loop
+// sleeps in its polls (the forward kernels and the plain backward gained
+// 1-2.5 % by it); the inline one does not (the dropout backward lost 2.5 %
+// with sleeping polls).
 __device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& wc,
                                           uint32_t site) {
   if (mbar_try_wait(bar, parity)) return;
@@ -154,7 +174,7 @@ __device__ __forceinline__ void mbar_wait_t(uint64_t* bar, uint32_t parity, cons
                                             uint32_t site) {
   if (mbar_try_wait(bar, parity)) return;
   if constexpr (kInline)
-    mbar_wait_poll(bar, parity, wc, site);
+    mbar_wait_poll<false>(bar, parity, wc, site);
   else
     mbar_wait_slow(bar, parity, wc, site);
 }
